@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized MoE layer forward (ds4moe) on GB300.
+
+One step = one full forward (router, bucketing, gate/up + SwiGLU, down, combine, shared
+expert) over one batch of synthetic tokens, inputs resident in HBM. L2 is flushed between
+steps (a write of twice the L2 size, outside the timed events). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+--config picks the workload (default 1: decode of one token, d=4096, 256 experts, top-8,
+f=2048, Q2_K routed + Q8_0 shared). Under torchrun each rank runs an independent replica on
+its own tokens (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")  # the CPU baseline is the single-threaded oracle
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "MoE layer tok/s; decode weight GB/s vs HBM peak; prefill TFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            pk = json.load(fh)
+        return dict(hbm=float(pk["hbm_gbs"]), bf16=float(pk["bf16_tflops"]),
+                    bf16_sus=float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sus=1700.0, src="fallback")
+
+
+def workload_name(spec: synthetic.Spec) -> str:
+    s = spec
+    txt = (f"{s.name}: {s.n_tokens} tokens, d={s.d}, {s.n_experts} experts top-{s.top_k}, f={s.f}, "
+           f"{s.fmt_gate_up}/{s.fmt_down} routed, {s.n_shared} {s.fmt_shared} shared f={s.f_shared}")
+    if s.bias:
+        txt += f", {s.bias} router bias"
+    if s.n_hash:
+        txt += f", first {s.n_hash} table-routed"
+    return txt
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def weight_bytes(spec, distinct: int) -> dict:
+    mgu = synthetic.row_bytes(spec.fmt_gate_up, spec.d) * spec.f
+    md = synthetic.row_bytes(spec.fmt_down, spec.f) * spec.d
+    shared = 0
+    if spec.n_shared:
+        shared = 2 * synthetic.row_bytes(spec.fmt_shared, spec.d) * spec.f_shared + \
+            synthetic.row_bytes(spec.fmt_shared, spec.f_shared) * spec.d
+    router = spec.n_experts * spec.d * 4 if spec.n_tokens > spec.n_hash else 0
+    return dict(routed_gateup=distinct * 2 * mgu, routed_down=distinct * md, shared=shared, router=router,
+                x=spec.n_tokens * spec.d * 2, out=spec.n_tokens * spec.d * 4)
+
+
+def forward_flops(spec) -> float:
+    per_pair = 2.0 * spec.d * spec.f * 3
+    shared = 2.0 * spec.d * spec.f_shared * 3 if spec.n_shared else 0.0
+    learned = spec.n_tokens - spec.n_hash
+    return spec.n_tokens * (spec.top_k * per_pair + shared) + learned * 2.0 * spec.n_experts * spec.d
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_moe_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(f"{workload}:{kernel}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.tmp.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.tmp.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+
+def oracle_sample(spec, problem, seconds: float, min_tokens: int = 1):
+    """Runs the fp64 oracle on successive tokens of the workload until `seconds` elapse."""
+    from oracle import moe
+    x = problem.x_bits
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_tokens or time.perf_counter() - t0 < seconds:
+        if n >= x.shape[0]:
+            break
+        moe.forward(problem, tokens=[n])
+        n += 1
+    dt = time.perf_counter() - t0
+    return n, dt
+
+
+def run_reference(args, spec, rank):
+    if rank != 0:
+        return
+    problem = synthetic.make_problem(spec)
+    # one step = one token of the workload through the oracle (bounded sample)
+    from oracle import moe
+    tok = 0
+
+    def step():
+        nonlocal tok
+        moe.forward(problem, tokens=[tok % spec.n_tokens])
+        tok += 1
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(spec), "sample": "one token per step"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} single-token forwards of the workload, fp64 numpy, 1 thread"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches", type=int, default=8, help="distinct input batches cycled over the steps")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = synthetic.CONFIGS[args.config]
+
+    if args.impl == "reference":
+        run_reference(args, spec, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from quantized_moe_gb300 import ds4moe as api
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    problem = synthetic.make_problem(spec)
+    shapes = api.make_shapes(spec.d, spec.f, spec.f_shared, spec.n_experts, spec.top_k, spec.n_shared,
+                             spec.fmt_gate_up, spec.fmt_down, spec.fmt_shared, problem.router_b is not None,
+                             spec.hash_vocab, spec.n_tokens, local)
+    arrays = [problem.router_w, problem.router_b, problem.gate.full(), problem.up.full(), problem.down.full(),
+              problem.shared_gate, problem.shared_up, problem.shared_down, problem.hash_table]
+    h = api.ds4moe_create(api.make_weights(*arrays), shapes)
+    del arrays
+
+    # per-rank input batches (different tokens per step, and per rank)
+    xs, tids = [], []
+    for b in range(args.batches):
+        sb = spec.with_(seed=spec.seed + 7919 * (rank * args.batches + b + 1))
+        xs.append(torch.from_numpy(synthetic.activations(sb).view(np.int16)).to(dev))
+        if spec.n_hash:
+            r = np.random.default_rng(sb.seed)
+            tids.append(torch.from_numpy(r.integers(0, spec.hash_vocab, spec.n_hash).astype(np.int32)).to(dev))
+    out = torch.empty((spec.n_tokens, spec.d), dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def fwd(i):
+        b = i % args.batches
+        api.ds4moe_forward_ex(h, xs[b].data_ptr(), spec.n_tokens, tids[b].data_ptr() if spec.n_hash else None,
+                              spec.n_hash, out.data_ptr(), stream.cuda_stream)
+
+    for i in range(args.warmup):
+        flush_buf.zero_()
+        fwd(i)
+    torch.cuda.synchronize()
+
+    # timed region: each step timed alone with events on the launching stream, L2 flushed between
+    api.ds4moe_set_profiling(h, True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    phase_ms: dict[str, list] = {}
+    distinct = []
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(args.steps):
+        flush_buf.zero_()
+        starts[i].record(stream)
+        fwd(i)
+        ends[i].record(stream)
+        for name, ms in api.ds4moe_get_phase_times(h):  # waits for this step
+            phase_ms.setdefault(name, []).append(ms)
+        distinct.append(api.ds4moe_get_stats(h)["distinct_experts"])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    api.ds4moe_set_profiling(h, False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = world * spec.n_tokens * args.steps
+    value = tokens / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+
+    # end to end through the host entry point: pinned host input, copies inside the timed region
+    x_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.int16, pin_memory=True)
+    x_host.copy_(xs[0].cpu())
+    out_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.float32, pin_memory=True)
+    tid_host = tids[0].cpu().pin_memory() if spec.n_hash else None
+    e2e_s = []
+    for i in range(args.warmup + args.steps):
+        flush_buf.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        api.ds4moe_forward_host(h, x_host.data_ptr(), spec.n_tokens, tid_host.data_ptr() if tid_host is not None else None,
+                                spec.n_hash, out_host.data_ptr(), stream.cuda_stream)
+        if i >= args.warmup:
+            e2e_s.append(time.perf_counter() - t0)
+    e2e_total = float(sum(e2e_s))
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = tokens / e2e_total
+
+    launches = api.ds4moe_launches_per_forward(h, spec.n_tokens) * args.steps
+    api.ds4moe_destroy(h)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # roofline of the dominant kernel (largest share of the stream time)
+    mean_phase = {k: float(np.mean(v)) for k, v in phase_ms.items()}
+    top = max(mean_phase, key=mean_phase.get)
+    d_mean = float(np.mean(distinct))
+    wb = weight_bytes(spec, d_mean)
+    flops = forward_flops(spec)
+    bytes_alg = {"routed_gateup": wb["routed_gateup"] + wb["x"], "routed_down": wb["routed_down"],
+                 "shared_gateup": wb["shared"] * 2 / 3 + wb["x"], "shared_down": wb["shared"] / 3,
+                 "router_logits": wb["router"] + wb["x"], "combine": wb["out"]}
+    decode = spec.n_tokens <= 64
+    if decode:
+        achieved = bytes_alg.get(top, 0.0) / (mean_phase[top] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm"], "peak_source": f"{peaks['src']} hbm_gbs",
+                "algorithmic_bytes_per_launch": bytes_alg.get(top, 0.0),
+                "traffic": recorded_traffic(top, spec.name)}
+    else:
+        pair = 2.0 * spec.d * spec.f
+        fl = {"routed_gateup": spec.n_tokens * spec.top_k * 2 * pair, "routed_down": spec.n_tokens * spec.top_k * pair,
+              "shared_gateup": spec.n_tokens * 2 * 2.0 * spec.d * spec.f_shared,
+              "shared_down": spec.n_tokens * 2.0 * spec.d * spec.f_shared}
+        achieved = fl.get(top, 0.0) / (mean_phase[top] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"], "peak_source": f"{peaks['src']} bf16_tflops (fp16 dense = bf16 rate)",
+                "algorithmic_flops_per_launch": fl.get(top, 0.0), "traffic": recorded_traffic(top, spec.name)}
+    fwd_bytes = sum(wb.values())
+    share = {k: v / sum(mean_phase.values()) for k, v in mean_phase.items()}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_done, dt = oracle_sample(spec, problem, args.cpu_seconds)
+        cpu = {"value": n_done / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n_done} token(s) of the workload, one at a time, fp64 numpy oracle, 1 thread "
+                         f"of {os.cpu_count()} host cores, {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 mma, f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_name(spec), "l2": "flushed between steps (write of 2x L2)",
+                   "parallelism": f"replicas x{world}", "batches": args.batches},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": spec.n_tokens * spec.d * 2 + spec.n_hash * 4,
+                "d2h_bytes_per_step": spec.n_tokens * spec.d * 4},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "detail": {"step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+                   "phase_ms": mean_phase, "phase_share": share, "distinct_experts_mean": d_mean,
+                   "forward_algorithmic_bytes": fwd_bytes, "forward_gbs": fwd_bytes / (ms_per_step / 1e3) / 1e9,
+                   "forward_hbm_frac": fwd_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm"],
+                   "forward_flops": flops, "forward_tflops": flops / (ms_per_step / 1e3) / 1e12,
+                   "kernel_source_hash": kernel_source_hash(), "peaks": peaks},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

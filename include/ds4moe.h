@@ -1,0 +1,162 @@
+/*
+ * ds4moe -- forward pass of a DeepSeek-V4-style quantized Mixture-of-Experts layer on one
+ * NVIDIA GB300 (sm_103a). C ABI: plain pointers and sizes, no C++ or framework types.
+ *
+ * What one forward computes, for each token x (a row of d bf16 values):
+ *
+ *   learned routing   z = W_r x + b (fp32), s = sigmoid(z); the top_k experts by
+ *                     (s descending, expert index ascending); w_j = s_j / sum of the
+ *                     selected s. The bias b (optional) is added before the sigmoid.
+ *   table routing     for the first n_hash tokens of a call: experts = table[token id],
+ *                     w_j = 1 / top_k (arc PR #89 "expert parallelism stage 0 + stage 1
+ *                     (EP=2) for V4's MoE", section "Stage 0": early layers route by a
+ *                     fixed token-id table).
+ *   routed experts    E_e(x) = W_d (silu(W_g x) * (W_u x)), weights dequantized from
+ *                     Q2_K or Q8_0 blocks inside the kernels.
+ *   combine           out = sum_j w_j E_{e_j}(x) + S(x): routed terms in ascending expert
+ *                     id, then the shared expert S (same SwiGLU form, unscaled), all fp32,
+ *                     fixed order, no floating-point atomics, so repeated calls are
+ *                     bitwise identical. The plain-sum combine is the one the expert
+ *                     parallel page describes (arc PR #89, section "Stage 1 -- EP=2"); its
+ *                     bitwise repeatability answers the scheduling-dependent float
+ *                     atomicAdd down projection recorded in TrevorS/ds4 PR #13 ("Tested").
+ *
+ * Tensor mix (ds4 PR #754 "CUDA: add DGX Spark network expert/tensor parallelism", section
+ * "Supported paths and safety"): 2-bit Q2_K routed experts, Q8_0 shared expert. Each of
+ * routed gate/up, routed down and shared may be either format.
+ *
+ * Canonical weight bytes accepted by ds4moe_create (little endian). A quantized [R x K]
+ * matrix is R rows, each row its K/block blocks back to back; a routed stack is n_experts
+ * such matrices back to back.
+ *   DS4MOE_FMT_Q8_0: block of 32 weights, 34 bytes = fp16 scale, 32 x int8 q; w = scale*q.
+ *   DS4MOE_FMT_Q2_K: super-block of 256 weights, 84 bytes = 16 scale bytes (byte j: low
+ *     nibble s_j, high nibble m_j, sub-block j = weights 16j..16j+15), 64 quant bytes
+ *     (weight i at byte i>>2, bits 2*(i&3)), fp16 d, fp16 dmin; w_i = d*s_j*q_i - dmin*m_j.
+ *
+ * Shapes: routed gate/up are [f_routed x d], routed down [d x f_routed], shared gate/up
+ * [f_shared x d], shared down [d x f_shared]. Every K dimension must be a multiple of 256
+ * for Q2_K and of 128 for Q8_0; d, f_routed and f_shared must be multiples of 128.
+ *
+ * Error convention: every int-returning call returns DS4MOE_OK (0) or a negative code and
+ * records a message readable with ds4moe_last_error() on the calling thread. Device-side
+ * faults (none are expected) surface at the caller's next synchronisation.
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4MOE_OK 0
+#define DS4MOE_ERR_INVALID_ARG -1        /* null pointer, bad size or shape */
+#define DS4MOE_ERR_UNSUPPORTED_FORMAT -2 /* format enum not Q8_0 / Q2_K, or shape not tileable */
+#define DS4MOE_ERR_DEVICE_MISMATCH -3    /* a device pointer lives on another GPU than the handle */
+#define DS4MOE_ERR_CAPACITY -4           /* n_tokens > max_tokens given at create */
+#define DS4MOE_ERR_OOM -5                /* device allocation failed or exceeded workspace_limit */
+#define DS4MOE_ERR_CUDA -6               /* a CUDA runtime call failed */
+
+typedef enum ds4moe_format { DS4MOE_FMT_Q8_0 = 0, DS4MOE_FMT_Q2_K = 1 } ds4moe_format;
+
+typedef struct ds4moe_shapes {
+    int32_t d;             /* hidden size */
+    int32_t f_routed;      /* routed expert intermediate size */
+    int32_t f_shared;      /* shared expert intermediate size (ignored when n_shared == 0) */
+    int32_t n_experts;     /* routed experts E, 1..256 */
+    int32_t top_k;         /* experts per token, 1..min(E, 16) */
+    int32_t n_shared;      /* 0 or 1 always-on shared expert */
+    int32_t fmt_gate_up;   /* ds4moe_format of the routed gate and up projections */
+    int32_t fmt_down;      /* ds4moe_format of the routed down projection */
+    int32_t fmt_shared;    /* ds4moe_format of the shared expert's three projections */
+    int32_t has_bias;      /* 1: router_b is read */
+    int32_t hash_vocab;    /* rows of the token-id routing table; 0 = no table routing */
+    int32_t max_tokens;    /* largest n_tokens of any later forward; sizes the workspace */
+    int32_t device;        /* CUDA device ordinal the handle lives on */
+    int32_t reserved;
+    int64_t workspace_limit; /* bytes; 0 = unlimited. Exceeding it returns DS4MOE_ERR_OOM */
+} ds4moe_shapes;
+
+/* Each pointer may be host memory (pageable or pinned) or device memory on shapes.device.
+ * ds4moe_create copies and repacks everything; the caller keeps ownership and may free or
+ * reuse its buffers as soon as the call returns. */
+typedef struct ds4moe_weights {
+    const float* router_w;      /* fp32 [E x d] row-major */
+    const float* router_b;      /* fp32 [E], read when has_bias, else may be NULL */
+    const void* gate;           /* routed gate stack, E x [f_routed x d] canonical blocks */
+    const void* up;             /* routed up stack, same shape */
+    const void* down;           /* routed down stack, E x [d x f_routed] */
+    const void* shared_gate;    /* [f_shared x d], NULL when n_shared == 0 */
+    const void* shared_up;      /* [f_shared x d] */
+    const void* shared_down;    /* [d x f_shared] */
+    const int32_t* hash_table;  /* int32 [hash_vocab x top_k], distinct ids per row; NULL if none */
+} ds4moe_weights;
+
+typedef struct ds4moe_stats {
+    int32_t n_tokens;          /* tokens of the last forward */
+    int32_t distinct_experts;  /* routed experts with at least one token in the last forward */
+    int32_t error_flags;       /* bit 0: a token id was outside [0, hash_vocab) (that token's
+                                  routed part was skipped) */
+    int32_t reserved;
+    int32_t counts[256];       /* tokens per routed expert in the last forward */
+} ds4moe_stats;
+
+typedef struct ds4moe_handle ds4moe_handle;
+
+/* Validates shapes, allocates the device weights and a workspace for max_tokens, copies and
+ * repacks the weights. Synchronous. On failure *out is set to NULL and nothing leaks. */
+int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out);
+
+/* Learned routing for every token. x: device bf16 [n_tokens x d]; out: device fp32
+ * [n_tokens x d]; both caller-owned, on the handle's device. stream: a cudaStream_t (NULL =
+ * legacy default stream). Asynchronous and stream-ordered: no host synchronisation. A handle
+ * serves one stream at a time (its workspace is shared by all calls on it). n_tokens == 0 is
+ * a no-op. */
+int ds4moe_forward(ds4moe_handle* h, const void* x, int32_t n_tokens, float* out, void* stream);
+
+/* As ds4moe_forward, but tokens 0..n_hash-1 take table routing by token_ids (device int32
+ * [n_hash]). n_hash must be 0 when the handle has no table. */
+int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n_tokens, const int32_t* token_ids,
+                      int32_t n_hash, float* out, void* stream);
+
+/* As ds4moe_forward_ex with host buffers: copies x (and token_ids) to the device, runs the
+ * forward and copies out back, then synchronises the stream before returning. */
+int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t n_tokens,
+                        const int32_t* token_ids_host, int32_t n_hash, float* out_host, void* stream);
+
+/* Copies the last forward's routing to host arrays idx [n_tokens x top_k] and w
+ * [n_tokens x top_k] in top-k order (score descending). Synchronises the handle's last
+ * stream; meant for tests and measurement, not for a timed path. */
+int ds4moe_get_route(ds4moe_handle* h, int32_t* idx_host, float* w_host, int32_t n_tokens);
+
+/* Per-expert token counts, distinct experts touched and error flags of the last forward.
+ * Synchronises like ds4moe_get_route. */
+int ds4moe_get_stats(ds4moe_handle* h, ds4moe_stats* st);
+
+/* Bytes of device memory the handle holds (weights + workspace). */
+int64_t ds4moe_device_bytes(const ds4moe_handle* h);
+
+/* Number of kernel launches one forward of n_tokens learned-routed tokens issues. */
+int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n_tokens);
+
+/* Per-launch timing for measurement: when enabled, every later forward records a CUDA event
+ * after each kernel launch on its stream (this adds event records between launches).
+ * ds4moe_get_phase_times waits for the last profiled forward and returns, for each launch in
+ * order, its stream time in milliseconds (ms, may be NULL) and a static name (names, may be
+ * NULL); *n_phases receives the number of launches (0 when profiling is off). */
+int ds4moe_set_profiling(ds4moe_handle* h, int32_t enable);
+int ds4moe_get_phase_times(ds4moe_handle* h, float* ms, const char** names, int32_t max_phases,
+                           int32_t* n_phases);
+
+/* Frees everything the handle owns. NULL is allowed. Synchronises the device first. */
+void ds4moe_destroy(ds4moe_handle* h);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* ds4moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4MOE_H */

@@ -84,11 +84,10 @@ def dequant_q2_k(row_bytes: np.ndarray, k: int) -> np.ndarray:
     m = (blk[:, :, 0:16] >> 4).astype(np.float64)
     qb = blk[:, :, 16:80]                                           # [rows, nb, 64]
     shifts = np.array([0, 2, 4, 6], dtype=np.uint8)
-    q = ((qb[:, :, :, None] >> shifts) & 3).reshape(rows, nb, 256).astype(np.float64)
+    q = ((qb[:, :, :, None] >> shifts) & 3).reshape(rows, nb, 16, 16)  # [.., sub-block j, i % 16]
     d = _f16(blk[:, :, 80:82])[:, :, None]                          # [rows, nb, 1]
     dmin = _f16(blk[:, :, 82:84])[:, :, None]
-    sub = np.arange(256) // 16
-    w = d * s[:, :, sub] * q - dmin * m[:, :, sub]
+    w = q * (d * s)[..., None] - (dmin * m)[..., None]
     return w.reshape(rows, k)
 
 

@@ -1,0 +1,57 @@
+// Deterministic combine: out[t] = sum over the token's routed slots, in ascending expert id,
+// of w_j * Y[position of slot j], then + the shared expert's row, all fp32, no atomics.
+#include "common.cuh"
+
+namespace ds4 {
+namespace {
+
+constexpr int kMaxK = 16;
+
+__global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ idx, const float* __restrict__ wts,
+                                                      const int* __restrict__ rowof, const float* __restrict__ y,
+                                                      const float* __restrict__ ys, int top_k, int d,
+                                                      float* __restrict__ out) {
+  __shared__ int s_pos[kMaxK];
+  __shared__ float s_w[kMaxK];
+  const int t = blockIdx.y;
+  if (threadIdx.x == 0) {
+    int e[kMaxK], p[kMaxK];
+    float w[kMaxK];
+    for (int j = 0; j < top_k; ++j) {  // insertion sort by expert id (ids are distinct)
+      const int ej = idx[t * top_k + j];
+      const float wj = wts[t * top_k + j];
+      const int pj = rowof[t * top_k + j];
+      int i = j;
+      while (i > 0 && e[i - 1] > ej) { e[i] = e[i - 1]; w[i] = w[i - 1]; p[i] = p[i - 1]; --i; }
+      e[i] = ej; w[i] = wj; p[i] = pj;
+    }
+    for (int j = 0; j < top_k; ++j) { s_pos[j] = p[j]; s_w[j] = w[j]; }
+  }
+  __syncthreads();
+  const int i4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < top_k; ++j) {
+    const float4 v = *reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4);
+    const float w = s_w[j];
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  if (ys) {
+    const float4 v = *reinterpret_cast<const float4*>(ys + (size_t)t * d + i4);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  *reinterpret_cast<float4*>(out + (size_t)t * d + i4) = acc;
+}
+
+}  // namespace
+
+void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
+                    int top_k, int d, float* out, cudaStream_t s) {
+  dim3 grid((d / 4 + 255) / 256, n_tok);
+  combine_kernel<<<grid, 256, 0, s>>>(idx, wts, rowof, y, ys, top_k, d, out);
+}
+
+}  // namespace ds4

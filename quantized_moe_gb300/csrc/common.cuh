@@ -1,0 +1,155 @@
+// Shared definitions of the ds4moe CUDA library: repacked weight layouts, launch helpers
+// and the warp-level MMA wrapper. Device code targets sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ds4 {
+
+// ----------------------------------------------------------------------------- layouts
+//
+// Quantized matrices are repacked at create time into "units" of 16 rows (a row-group)
+// by one K-chunk, ordered tile-major: [row-tile of 128 rows][K-unit][row-group in tile][unit].
+// Inside a unit every warp lane finds the bits of its m16n8k16 A fragments contiguous, so a
+// warp streams a unit with coalesced 16-byte loads.
+//
+// Fragment map of mma.m16n8k16 (lane = 4*g + t): A register r holds row g + 8*(r&1) at
+// k = 2t + 8*(r>>1) (low half) and k+1 (high half); B register r holds k = 2t + 8*r (+1)
+// of column g; C element c holds row g + 8*(c>>1), column 2t + (c&1).
+//
+// Q2_K unit = 16 rows x 256 k (one super-block per row), 1344 bytes:
+//   [0, 1024)    quants of k-chunk 0 then k-chunk 1 (128 k each). In a chunk lane L owns
+//                bytes [16L, 16L+16) = 4 words; word r holds, for MMA i = 0..7 (sub-block
+//                8c+i), the 2-bit q of A register r at bits [2i, 2i+2) (low half, k) and
+//                [16+2i, 18+2i) (high half, k+1).
+//   [1024, 1280) scale bytes of chunk 0 then chunk 1, lane L owns bytes [4L, 4L+4):
+//                (row g, sub 2t), (row g, sub 2t+1), (row g+8, sub 2t), (row g+8, sub 2t+1),
+//                sub counted inside the chunk; each byte keeps s in the low nibble, m high.
+//   [1280, 1344) row r (0..15): fp16 d, fp16 dmin.
+// Q8_0 unit = 16 rows x 128 k (four blocks per row), 2176 bytes:
+//   [0, 2048)    u = q + 128 as bytes. Load j = 0..3 covers MMAs 2j, 2j+1: lane L owns
+//                bytes [512j + 16L, +16): word 2m+h holds A registers 2h, 2h+1 of MMA 2j+m
+//                as (reg 2h low, reg 2h high, reg 2h+1 low, reg 2h+1 high) bytes.
+//   [2048, 2176) lane L owns bytes [4L, 4L+4): fp16 scale of (row g, block t), (row g+8, block t).
+constexpr int kRowGroup = 16;
+constexpr int kTileRows = 128;
+constexpr int kQ2kUnitK = 256;
+constexpr int kQ2kUnitBytes = 1344;
+constexpr int kQ2kScOff = 1024;
+constexpr int kQ2kDdOff = 1280;
+constexpr int kQ80UnitK = 128;
+constexpr int kQ80UnitBytes = 2176;
+constexpr int kQ80ScOff = 2048;
+
+enum Fmt : int { FMT_Q8_0 = 0, FMT_Q2_K = 1 };
+
+__host__ __device__ constexpr int unit_k(int fmt) { return fmt == FMT_Q2_K ? kQ2kUnitK : kQ80UnitK; }
+__host__ __device__ constexpr int unit_bytes(int fmt) { return fmt == FMT_Q2_K ? kQ2kUnitBytes : kQ80UnitBytes; }
+__host__ __device__ constexpr int canon_block(int fmt) { return fmt == FMT_Q2_K ? 256 : 32; }
+__host__ __device__ constexpr int canon_block_bytes(int fmt) { return fmt == FMT_Q2_K ? 84 : 34; }
+
+// Byte offset of unit (row-group rg, K-unit kb) in a repacked matrix with n_kb K-units.
+__host__ __device__ inline size_t unit_offset(int rg, int kb, int n_kb, int ubytes) {
+  const int tile = rg >> 3, rgi = rg & 7;
+  return ((size_t)(tile * n_kb + kb) * 8 + rgi) * (size_t)ubytes;
+}
+
+// Bytes of one repacked (or canonical: the sizes agree) [rows x k] matrix.
+__host__ __device__ inline size_t matrix_bytes(int fmt, int rows, int k) {
+  return (size_t)rows * (size_t)(k / canon_block(fmt)) * canon_block_bytes(fmt);
+}
+
+// ----------------------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Power-of-two scale that maps a row maximum into [2^14, 2^15) so the row converts to fp16
+// without overflow; exact (only the exponent changes). Returns 1 for an all-zero row.
+__device__ __forceinline__ float fp16_row_scale(float amax) {
+  if (!(amax > 0.f) || !isfinite(amax)) return 1.f;
+  int e;
+  frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
+  return ldexpf(1.f, 15 - e);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+}  // namespace ds4
+
+// ----------------------------------------------------------------------------- host launchers
+// (defined in the kernel translation units, called by the C-ABI shim)
+
+namespace ds4 {
+
+struct GemvArgs {
+  const uint8_t* w0;        // repacked stack (gate, or down)
+  const uint8_t* w1;        // repacked stack (up); unused by the down kernel
+  size_t mat_bytes;         // bytes of one expert's matrix
+  int rows;                 // output rows per matrix (f for gate/up, d for down)
+  int k;                    // reduction length (d for gate/up, f for down)
+  const int* active;        // active expert list (routed) or nullptr (shared)
+  const int* n_active;      // device count of active experts (routed)
+  const int* offsets;       // [E+1] bucketed offsets (routed)
+  const int* perm;          // bucketed position -> flat slot id t*top_k + j (routed)
+  int top_k;
+  int n_tokens;             // shared: tokens of this call
+  const __nv_bfloat16* x;   // gate/up input [n_tokens x k]
+  const float* hin;         // down input rows [pos x k] (routed: bucketed positions, shared: tokens)
+  float* out;               // gate/up: H [pos x rows]; down: Y [pos x rows]
+};
+
+void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s);
+void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float* w, const float* b, int n_exp,
+                          float* logits, cudaStream_t s);
+void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const int* token_ids, int n_hash,
+                 const int* table, int vocab, int* idx, float* wts, int* err, cudaStream_t s);
+void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* counts, cudaStream_t s);
+void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* counts, int* offsets, int* active,
+                           int* n_active, int* perm, int* rowof, cudaStream_t s);
+void launch_gateup(int fmt, const GemvArgs& a, int max_active, cudaStream_t s);
+void launch_down(int fmt, const GemvArgs& a, int max_active, cudaStream_t s);
+void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
+                    int top_k, int d, float* out, cudaStream_t s);
+
+}  // namespace ds4

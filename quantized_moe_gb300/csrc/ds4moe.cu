@@ -1,0 +1,480 @@
+// C-ABI shim of the ds4moe library: argument validation, device memory, create-time repack
+// and the launch sequence of one forward. Host code only; kernels live in the other units.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/ds4moe.h"
+#include "common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define DS4_CUDA(call)                                                                          \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) ok = true;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+enum PtrKind { PTR_HOST, PTR_DEVICE, PTR_OTHER_DEVICE };
+
+PtrKind classify(const void* p, int device) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();  // clear: an unknown pointer is plain host memory
+    return PTR_HOST;
+  }
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+    return attr.device == device ? PTR_DEVICE : PTR_OTHER_DEVICE;
+  return PTR_HOST;
+}
+
+}  // namespace
+
+struct ds4moe_handle {
+  ds4moe_shapes s{};
+  int64_t bytes = 0;
+  std::vector<void*> allocs;
+  // weights
+  float* router_w = nullptr;
+  float* router_b = nullptr;
+  uint8_t* gate = nullptr;
+  uint8_t* up = nullptr;
+  uint8_t* down = nullptr;
+  uint8_t* sgate = nullptr;
+  uint8_t* sup = nullptr;
+  uint8_t* sdown = nullptr;
+  int* table = nullptr;
+  size_t mb_gu = 0, mb_d = 0, mb_sgu = 0, mb_sd = 0;
+  // workspace
+  float* logits = nullptr;
+  int* idx = nullptr;
+  float* wts = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* active = nullptr;
+  int* n_active = nullptr;
+  int* perm = nullptr;
+  int* rowof = nullptr;
+  float* H = nullptr;
+  float* Hs = nullptr;
+  float* Y = nullptr;
+  float* Ys = nullptr;
+  int* err = nullptr;
+  // host-call staging
+  __nv_bfloat16* x_stage = nullptr;
+  int* tid_stage = nullptr;
+  float* out_stage = nullptr;
+  // last forward
+  cudaStream_t last_stream = nullptr;
+  int last_n = 0;
+  // optional per-launch timing (events recorded between launches on the forward's stream)
+  bool profile = false;
+  static constexpr int kMaxPhases = 16;
+  cudaEvent_t ev[kMaxPhases + 1] = {};
+  const char* phase_name[kMaxPhases] = {};
+  int n_phases = 0;
+
+  int alloc(void** p, size_t n) {
+    if (n == 0) n = 16;
+    if (s.workspace_limit > 0 && bytes + (int64_t)n > s.workspace_limit)
+      return fail(DS4MOE_ERR_OOM, "device allocation of %zu bytes exceeds workspace_limit %lld (held %lld)", n,
+                  (long long)s.workspace_limit, (long long)bytes);
+    cudaError_t e = cudaMalloc(p, n);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      *p = nullptr;
+      return fail(DS4MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", n, cudaGetErrorString(e));
+    }
+    allocs.push_back(*p);
+    bytes += (int64_t)n;
+    return DS4MOE_OK;
+  }
+  template <typename T>
+  int alloc_t(T** p, size_t n) {
+    return alloc(reinterpret_cast<void**>(p), n);
+  }
+  void release() {
+    for (cudaEvent_t& e : ev)
+      if (e) {
+        cudaEventDestroy(e);
+        e = nullptr;
+      }
+    for (void* p : allocs) cudaFree(p);
+    allocs.clear();
+    bytes = 0;
+  }
+};
+
+namespace {
+
+bool fmt_ok(int f) { return f == DS4MOE_FMT_Q8_0 || f == DS4MOE_FMT_Q2_K; }
+
+int check_shapes(const ds4moe_shapes* s) {
+  if (s->d <= 0 || s->d % 128 || s->d > 16384) return fail(DS4MOE_ERR_INVALID_ARG, "d=%d must be a positive multiple of 128 up to 16384", s->d);
+  if (s->f_routed <= 0 || s->f_routed % 128 || s->f_routed > 16384)
+    return fail(DS4MOE_ERR_INVALID_ARG, "f_routed=%d must be a positive multiple of 128 up to 16384", s->f_routed);
+  if (s->n_shared != 0 && s->n_shared != 1) return fail(DS4MOE_ERR_INVALID_ARG, "n_shared=%d must be 0 or 1", s->n_shared);
+  if (s->n_shared && (s->f_shared <= 0 || s->f_shared % 128 || s->f_shared > 16384))
+    return fail(DS4MOE_ERR_INVALID_ARG, "f_shared=%d must be a positive multiple of 128 up to 16384", s->f_shared);
+  if (s->n_experts < 1 || s->n_experts > 256) return fail(DS4MOE_ERR_INVALID_ARG, "n_experts=%d must be in 1..256", s->n_experts);
+  if (s->top_k < 1 || s->top_k > 16 || s->top_k > s->n_experts)
+    return fail(DS4MOE_ERR_INVALID_ARG, "top_k=%d must be in 1..min(n_experts, 16)", s->top_k);
+  if (s->max_tokens < 1 || s->max_tokens > 65535) return fail(DS4MOE_ERR_INVALID_ARG, "max_tokens=%d must be in 1..65535", s->max_tokens);
+  if (s->hash_vocab < 0) return fail(DS4MOE_ERR_INVALID_ARG, "hash_vocab=%d is negative", s->hash_vocab);
+  const int fm[3] = {s->fmt_gate_up, s->fmt_down, s->fmt_shared};
+  const char* nm[3] = {"fmt_gate_up", "fmt_down", "fmt_shared"};
+  for (int i = 0; i < 3; ++i)
+    if (!fmt_ok(fm[i]) && !(i == 2 && !s->n_shared))
+      return fail(DS4MOE_ERR_UNSUPPORTED_FORMAT, "%s=%d is not a supported block format (Q8_0=0, Q2_K=1)", nm[i], fm[i]);
+  auto kq = [](int fmt, int k) { return k % ds4::unit_k(fmt) == 0; };
+  if (!kq(s->fmt_gate_up, s->d)) return fail(DS4MOE_ERR_UNSUPPORTED_FORMAT, "d=%d is not a multiple of %d required by fmt_gate_up", s->d, ds4::unit_k(s->fmt_gate_up));
+  if (!kq(s->fmt_down, s->f_routed)) return fail(DS4MOE_ERR_UNSUPPORTED_FORMAT, "f_routed=%d is not a multiple of %d required by fmt_down", s->f_routed, ds4::unit_k(s->fmt_down));
+  if (s->n_shared && (!kq(s->fmt_shared, s->d) || !kq(s->fmt_shared, s->f_shared)))
+    return fail(DS4MOE_ERR_UNSUPPORTED_FORMAT, "shared expert K dims (d=%d, f_shared=%d) are not multiples of %d", s->d, s->f_shared, ds4::unit_k(s->fmt_shared));
+  return DS4MOE_OK;
+}
+
+int check_device(int device) {
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(DS4MOE_ERR_CUDA, "no CUDA device available");
+  }
+  if (device < 0 || device >= ndev) return fail(DS4MOE_ERR_INVALID_ARG, "device=%d out of range (%d devices)", device, ndev);
+  return DS4MOE_OK;
+}
+
+// Copies `bytes` from a host or device source into dst (device).
+int copy_in(void* dst, const void* src, size_t bytes, int device, const char* what) {
+  const PtrKind k = classify(src, device);
+  if (k == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than %d", what, device);
+  DS4_CUDA(cudaMemcpy(dst, src, bytes, k == PTR_DEVICE ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice));
+  return DS4MOE_OK;
+}
+
+// Repacks n_mat canonical [rows x k] matrices (back to back) into dst.
+int repack_stack(ds4moe_handle* h, int fmt, const void* src, uint8_t* dst, int n_mat, int rows, int k,
+                 const char* what) {
+  const size_t mb = ds4::matrix_bytes(fmt, rows, k);
+  const PtrKind kind = classify(src, h->s.device);
+  if (kind == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than %d", what, h->s.device);
+  if (kind == PTR_DEVICE) {
+    ds4::launch_repack(fmt, static_cast<const uint8_t*>(src), dst, n_mat * rows, k, 0);
+    DS4_CUDA(cudaGetLastError());
+    DS4_CUDA(cudaDeviceSynchronize());
+    return DS4MOE_OK;
+  }
+  // host source: stage a batch of matrices at a time (at most ~256 MB of staging)
+  int per = (int)std::max<size_t>(1, (size_t)(256u << 20) / mb);
+  per = std::min(per, n_mat);
+  uint8_t* stage = nullptr;
+  cudaError_t e = cudaMalloc(&stage, mb * per);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DS4MOE_ERR_OOM, "staging buffer of %zu bytes: %s", mb * per, cudaGetErrorString(e));
+  }
+  int rc = DS4MOE_OK;
+  for (int m0 = 0; m0 < n_mat && rc == DS4MOE_OK; m0 += per) {
+    const int n = std::min(per, n_mat - m0);
+    e = cudaMemcpy(stage, static_cast<const uint8_t*>(src) + mb * m0, mb * n, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+      ds4::launch_repack(fmt, stage, dst + mb * m0, n * rows, k, 0);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = fail(DS4MOE_ERR_CUDA, "repack of %s: %s", what, cudaGetErrorString(e));
+  }
+  cudaFree(stage);
+  return rc;
+}
+
+#define DS4_TRY(call)          \
+  do {                         \
+    int rc_ = (call);          \
+    if (rc_ != DS4MOE_OK) {    \
+      h->release();            \
+      delete h;                \
+      return rc_;              \
+    }                          \
+  } while (0)
+
+}  // namespace
+
+extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out) {
+  if (!out) return fail(DS4MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!w || !s) return fail(DS4MOE_ERR_INVALID_ARG, "weights or shapes is NULL");
+  int rc = check_shapes(s);
+  if (rc != DS4MOE_OK) return rc;
+  if (!w->router_w || !w->gate || !w->up || !w->down) return fail(DS4MOE_ERR_INVALID_ARG, "router_w, gate, up and down are required");
+  if (s->has_bias && !w->router_b) return fail(DS4MOE_ERR_INVALID_ARG, "has_bias set but router_b is NULL");
+  if (s->n_shared && (!w->shared_gate || !w->shared_up || !w->shared_down))
+    return fail(DS4MOE_ERR_INVALID_ARG, "n_shared=1 but a shared expert tensor is NULL");
+  if (s->hash_vocab > 0 && !w->hash_table) return fail(DS4MOE_ERR_INVALID_ARG, "hash_vocab>0 but hash_table is NULL");
+  rc = check_device(s->device);
+  if (rc != DS4MOE_OK) return rc;
+  DeviceGuard guard(s->device);
+  if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", s->device);
+
+  ds4moe_handle* h = new ds4moe_handle();
+  h->s = *s;
+  const int E = s->n_experts, d = s->d, f = s->f_routed, fs = s->f_shared, K = s->top_k;
+  h->mb_gu = ds4::matrix_bytes(s->fmt_gate_up, f, d);
+  h->mb_d = ds4::matrix_bytes(s->fmt_down, d, f);
+  // weights
+  DS4_TRY(h->alloc_t(&h->router_w, (size_t)E * d * 4));
+  DS4_TRY(copy_in(h->router_w, w->router_w, (size_t)E * d * 4, s->device, "router_w"));
+  if (s->has_bias) {
+    DS4_TRY(h->alloc_t(&h->router_b, (size_t)E * 4));
+    DS4_TRY(copy_in(h->router_b, w->router_b, (size_t)E * 4, s->device, "router_b"));
+  }
+  DS4_TRY(h->alloc_t(&h->gate, h->mb_gu * E));
+  DS4_TRY(h->alloc_t(&h->up, h->mb_gu * E));
+  DS4_TRY(h->alloc_t(&h->down, h->mb_d * E));
+  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->gate, h->gate, E, f, d, "gate"));
+  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->up, h->up, E, f, d, "up"));
+  DS4_TRY(repack_stack(h, s->fmt_down, w->down, h->down, E, d, f, "down"));
+  if (s->n_shared) {
+    h->mb_sgu = ds4::matrix_bytes(s->fmt_shared, fs, d);
+    h->mb_sd = ds4::matrix_bytes(s->fmt_shared, d, fs);
+    DS4_TRY(h->alloc_t(&h->sgate, h->mb_sgu));
+    DS4_TRY(h->alloc_t(&h->sup, h->mb_sgu));
+    DS4_TRY(h->alloc_t(&h->sdown, h->mb_sd));
+    DS4_TRY(repack_stack(h, s->fmt_shared, w->shared_gate, h->sgate, 1, fs, d, "shared_gate"));
+    DS4_TRY(repack_stack(h, s->fmt_shared, w->shared_up, h->sup, 1, fs, d, "shared_up"));
+    DS4_TRY(repack_stack(h, s->fmt_shared, w->shared_down, h->sdown, 1, d, fs, "shared_down"));
+  }
+  if (s->hash_vocab > 0) {
+    DS4_TRY(h->alloc_t(&h->table, (size_t)s->hash_vocab * K * 4));
+    DS4_TRY(copy_in(h->table, w->hash_table, (size_t)s->hash_vocab * K * 4, s->device, "hash_table"));
+  }
+  // workspace for max_tokens
+  const size_t M = (size_t)s->max_tokens, slots = M * K;
+  DS4_TRY(h->alloc_t(&h->logits, M * E * 4));
+  DS4_TRY(h->alloc_t(&h->idx, slots * 4));
+  DS4_TRY(h->alloc_t(&h->wts, slots * 4));
+  DS4_TRY(h->alloc_t(&h->counts, (size_t)E * 4));
+  DS4_TRY(h->alloc_t(&h->offsets, (size_t)(E + 1) * 4));
+  DS4_TRY(h->alloc_t(&h->active, (size_t)E * 4));
+  DS4_TRY(h->alloc_t(&h->n_active, 4));
+  DS4_TRY(h->alloc_t(&h->perm, slots * 4));
+  DS4_TRY(h->alloc_t(&h->rowof, slots * 4));
+  DS4_TRY(h->alloc_t(&h->H, slots * f * 4));
+  DS4_TRY(h->alloc_t(&h->Y, slots * d * 4));
+  if (s->n_shared) {
+    DS4_TRY(h->alloc_t(&h->Hs, M * fs * 4));
+    DS4_TRY(h->alloc_t(&h->Ys, M * d * 4));
+  }
+  DS4_TRY(h->alloc_t(&h->err, 4));
+  DS4_TRY(h->alloc_t(&h->x_stage, M * d * 2));
+  DS4_TRY(h->alloc_t(&h->tid_stage, M * 4));
+  DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
+  cudaError_t e = cudaMemset(h->err, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    rc = fail(DS4MOE_ERR_CUDA, "workspace init: %s", cudaGetErrorString(e));
+    h->release();
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, const int32_t* token_ids,
+                                 int32_t n_hash, float* out, void* stream) {
+  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+  const ds4moe_shapes& s = h->s;
+  if (n < 0) return fail(DS4MOE_ERR_INVALID_ARG, "n_tokens=%d is negative", n);
+  if (n > s.max_tokens) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d exceeds max_tokens=%d", n, s.max_tokens);
+  if (n_hash < 0 || n_hash > n) return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d must be in 0..n_tokens", n_hash);
+  if (n_hash > 0 && (s.hash_vocab == 0 || !token_ids))
+    return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d needs a handle with a hash table and token_ids", n_hash);
+  if (n == 0) return DS4MOE_OK;
+  if (!x || !out) return fail(DS4MOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return fail(DS4MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  const void* ptrs[3] = {x, out, n_hash ? token_ids : nullptr};
+  const char* names[3] = {"x", "out", "token_ids"};
+  for (int i = 0; i < 3; ++i) {
+    if (!ptrs[i]) continue;
+    const PtrKind k = classify(ptrs[i], s.device);
+    if (k == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than the handle's (%d)", names[i], s.device);
+    if (k != PTR_DEVICE) return fail(DS4MOE_ERR_INVALID_ARG, "%s is not device memory (use ds4moe_forward_host for host buffers)", names[i]);
+  }
+  DeviceGuard guard(s.device);
+  if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", s.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int E = s.n_experts, K = s.top_k, d = s.d, f = s.f_routed, fs = s.f_shared;
+  const int n_learned = n - n_hash;
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
+  int phase = 0;
+  if (h->profile) DS4_CUDA(cudaEventRecord(h->ev[0], st));
+  auto mark = [&](const char* name) {
+    if (h->profile && phase < ds4moe_handle::kMaxPhases) {
+      h->phase_name[phase] = name;
+      cudaEventRecord(h->ev[++phase], st);
+    }
+  };
+  if (n_learned > 0) {
+    ds4::launch_router_logits(xb + (size_t)n_hash * d, n_learned, d, h->router_w, h->router_b, E, h->logits, st);
+    mark("router_logits");
+  }
+  ds4::launch_topk(h->logits, n_learned, E, K, token_ids, n_hash, h->table, s.hash_vocab, h->idx, h->wts, h->err, st);
+  mark("topk");
+  ds4::launch_bucket_count(h->idx, n * K, E, h->counts, st);
+  mark("bucket_count");
+  ds4::launch_bucket_scatter(h->idx, n * K, E, h->counts, h->offsets, h->active, h->n_active, h->perm, h->rowof, st);
+  mark("bucket_scatter");
+  const int max_active = std::min(E, n * K);
+  ds4::GemvArgs a{};
+  a.w0 = h->gate; a.w1 = h->up; a.mat_bytes = h->mb_gu; a.rows = f; a.k = d;
+  a.active = h->active; a.n_active = h->n_active; a.offsets = h->offsets; a.perm = h->perm; a.top_k = K;
+  a.n_tokens = n; a.x = xb; a.out = h->H;
+  ds4::launch_gateup(s.fmt_gate_up, a, max_active, st);
+  mark("routed_gateup");
+  ds4::GemvArgs dn = a;
+  dn.w0 = h->down; dn.w1 = nullptr; dn.mat_bytes = h->mb_d; dn.rows = d; dn.k = f; dn.hin = h->H; dn.out = h->Y;
+  ds4::launch_down(s.fmt_down, dn, max_active, st);
+  mark("routed_down");
+  if (s.n_shared) {
+    ds4::GemvArgs sa{};
+    sa.w0 = h->sgate; sa.w1 = h->sup; sa.mat_bytes = h->mb_sgu; sa.rows = fs; sa.k = d; sa.top_k = K;
+    sa.n_tokens = n; sa.x = xb; sa.out = h->Hs;
+    ds4::launch_gateup(s.fmt_shared, sa, 1, st);
+    mark("shared_gateup");
+    ds4::GemvArgs sd = sa;
+    sd.w0 = h->sdown; sd.w1 = nullptr; sd.mat_bytes = h->mb_sd; sd.rows = d; sd.k = fs; sd.hin = h->Hs; sd.out = h->Ys;
+    ds4::launch_down(s.fmt_shared, sd, 1, st);
+    mark("shared_down");
+  }
+  ds4::launch_combine(h->idx, h->wts, h->rowof, h->Y, s.n_shared ? h->Ys : nullptr, n, K, d, out, st);
+  mark("combine");
+  h->n_phases = phase;
+  DS4_CUDA(cudaGetLastError());
+  h->last_stream = st;
+  h->last_n = n;
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_forward(ds4moe_handle* h, const void* x, int32_t n, float* out, void* stream) {
+  return ds4moe_forward_ex(h, x, n, nullptr, 0, out, stream);
+}
+
+extern "C" int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t n, const int32_t* tid_host,
+                                   int32_t n_hash, float* out_host, void* stream) {
+  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (n < 0 || n > h->s.max_tokens)
+    return fail(n < 0 ? DS4MOE_ERR_INVALID_ARG : DS4MOE_ERR_CAPACITY, "n_tokens=%d outside 0..max_tokens=%d", n, h->s.max_tokens);
+  if (n == 0) return DS4MOE_OK;
+  if (!x_host || !out_host || (n_hash > 0 && !tid_host)) return fail(DS4MOE_ERR_INVALID_ARG, "x, out or token_ids is NULL");
+  DeviceGuard guard(h->s.device);
+  if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", h->s.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t d = (size_t)h->s.d;
+  DS4_CUDA(cudaMemcpyAsync(h->x_stage, x_host, (size_t)n * d * 2, cudaMemcpyHostToDevice, st));
+  if (n_hash > 0) DS4_CUDA(cudaMemcpyAsync(h->tid_stage, tid_host, (size_t)n_hash * 4, cudaMemcpyHostToDevice, st));
+  int rc = ds4moe_forward_ex(h, h->x_stage, n, n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage, stream);
+  if (rc != DS4MOE_OK) return rc;
+  DS4_CUDA(cudaMemcpyAsync(out_host, h->out_stage, (size_t)n * d * 4, cudaMemcpyDeviceToHost, st));
+  DS4_CUDA(cudaStreamSynchronize(st));
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_get_route(ds4moe_handle* h, int32_t* idx_host, float* w_host, int32_t n) {
+  if (!h || !idx_host || !w_host) return fail(DS4MOE_ERR_INVALID_ARG, "NULL argument");
+  if (n < 0 || n > h->last_n) return fail(DS4MOE_ERR_INVALID_ARG, "n_tokens=%d exceeds the last forward's %d", n, h->last_n);
+  DeviceGuard guard(h->s.device);
+  DS4_CUDA(cudaStreamSynchronize(h->last_stream));
+  const size_t sl = (size_t)n * h->s.top_k;
+  DS4_CUDA(cudaMemcpy(idx_host, h->idx, sl * 4, cudaMemcpyDeviceToHost));
+  DS4_CUDA(cudaMemcpy(w_host, h->wts, sl * 4, cudaMemcpyDeviceToHost));
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_get_stats(ds4moe_handle* h, ds4moe_stats* st) {
+  if (!h || !st) return fail(DS4MOE_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(h->s.device);
+  DS4_CUDA(cudaStreamSynchronize(h->last_stream));
+  memset(st, 0, sizeof *st);
+  st->n_tokens = h->last_n;
+  if (h->last_n > 0) {
+    DS4_CUDA(cudaMemcpy(st->counts, h->counts, (size_t)h->s.n_experts * 4, cudaMemcpyDeviceToHost));
+    DS4_CUDA(cudaMemcpy(&st->distinct_experts, h->n_active, 4, cudaMemcpyDeviceToHost));
+    DS4_CUDA(cudaMemcpy(&st->error_flags, h->err, 4, cudaMemcpyDeviceToHost));
+  }
+  return DS4MOE_OK;
+}
+
+extern "C" int64_t ds4moe_device_bytes(const ds4moe_handle* h) { return h ? h->bytes : 0; }
+
+extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n_tokens) {
+  if (!h || n_tokens <= 0) return 0;
+  // router, top-k, 2 bucketing, gate/up + down routed, the same for shared, combine
+  return 1 + 1 + 2 + 2 + (h->s.n_shared ? 2 : 0) + 1;
+}
+
+extern "C" int ds4moe_set_profiling(ds4moe_handle* h, int32_t enable) {
+  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+  DeviceGuard guard(h->s.device);
+  if (enable && !h->ev[0])
+    for (cudaEvent_t& e : h->ev) DS4_CUDA(cudaEventCreate(&e));
+  h->profile = enable != 0;
+  h->n_phases = 0;
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_get_phase_times(ds4moe_handle* h, float* ms, const char** names, int32_t max_phases,
+                                      int32_t* n_phases) {
+  if (!h || !n_phases) return fail(DS4MOE_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(h->s.device);
+  *n_phases = h->profile ? h->n_phases : 0;
+  if (*n_phases == 0) return DS4MOE_OK;
+  DS4_CUDA(cudaEventSynchronize(h->ev[h->n_phases]));
+  for (int i = 0; i < h->n_phases && i < max_phases; ++i) {
+    if (ms) DS4_CUDA(cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]));
+    if (names) names[i] = h->phase_name[i];
+  }
+  return DS4MOE_OK;
+}
+
+extern "C" void ds4moe_destroy(ds4moe_handle* h) {
+  if (!h) return;
+  DeviceGuard guard(h->s.device);
+  cudaDeviceSynchronize();
+  h->release();
+  delete h;
+}
+
+extern "C" const char* ds4moe_last_error(void) { return g_last_error.c_str(); }

@@ -1,0 +1,113 @@
+"""GPU: bitwise run-to-run determinism, placement invariance on the device, and the C-ABI
+error paths that need a device (capacity, pointer checks, workspace cap, bad token ids)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synthetic
+from oracle import moe
+import moe_gpu
+from quantized_moe_gb300 import ds4moe as api
+from test_gpu_parity import SMALL_MIX
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("spec,reps", [(synthetic.CONFIGS[1], 20), (SMALL_MIX, 20), (synthetic.CONFIGS[3], 5)],
+                         ids=lambda v: getattr(v, "name", str(v)))
+def test_repeated_forwards_are_bitwise_identical(spec, reps):
+    p = synthetic.make_problem(spec)
+    h = moe_gpu.create(p)
+    try:
+        first, idx0, w0 = moe_gpu.forward(h, p)
+        for _ in range(reps - 1):
+            out, idx, w = moe_gpu.forward(h, p)
+            assert np.array_equal(out.view(np.uint32), first.view(np.uint32))
+            assert np.array_equal(idx, idx0) and np.array_equal(w.view(np.uint32), w0.view(np.uint32))
+    finally:
+        api.ds4moe_destroy(h)
+
+
+def test_expert_placement_invariance_on_device():
+    p = synthetic.make_problem(SMALL_MIX)
+    perm = np.random.default_rng(9).permutation(SMALL_MIX.n_experts)
+    inv = np.argsort(perm)
+    st = lambda s: np.stack([s[int(inv[i])] for i in range(len(perm))])
+    q = dataclasses.replace(p, router_w=p.router_w[inv], router_b=p.router_b[inv], gate=st(p.gate), up=st(p.up),
+                            down=st(p.down), hash_table=perm[p.hash_table].astype(np.int32))
+    ha, hb = moe_gpu.create(p), moe_gpu.create(q)
+    try:
+        a, ia, _ = moe_gpu.forward(ha, p)
+        b, ib, _ = moe_gpu.forward(hb, q)
+    finally:
+        api.ds4moe_destroy(ha)
+        api.ds4moe_destroy(hb)
+    assert np.array_equal(np.sort(perm[ia], 1), np.sort(ib, 1))
+    assert np.max(np.abs(a - b)) <= moe_gpu.tolerance(a)
+
+
+def test_token_count_edges():
+    p = synthetic.make_problem(SMALL_MIX)
+    h = moe_gpu.create(p, max_tokens=64)
+    try:
+        import torch
+        x = torch.zeros((1, SMALL_MIX.d), dtype=torch.int16, device="cuda")
+        out = torch.zeros((1, SMALL_MIX.d), dtype=torch.float32, device="cuda")
+        api.ds4moe_forward(h, x.data_ptr(), 0, out.data_ptr(), 0)  # n = 0 is a no-op
+        with pytest.raises(api.Ds4MoeError) as ei:
+            api.ds4moe_forward(h, x.data_ptr(), 65, out.data_ptr(), 0)
+        assert ei.value.code == api.DS4MOE_ERR_CAPACITY
+        host = np.zeros((1, SMALL_MIX.d), np.uint16)
+        with pytest.raises(api.Ds4MoeError) as ei:
+            api.ds4moe_forward(h, host, 1, out.data_ptr(), 0)
+        assert ei.value.code == api.DS4MOE_ERR_INVALID_ARG
+        # all-zero activations: every learned score is 1/2, ties go to experts 0..k-1
+        got, idx, w = moe_gpu.forward(h, p, x_bits=np.zeros((3, SMALL_MIX.d), np.uint16), n_hash=0)
+        b = p.router_b.astype(np.float64)
+        want = np.argsort(-b, kind="stable")[:SMALL_MIX.top_k]
+        assert all(sorted(r) == sorted(want.tolist()) for r in idx.tolist())
+        assert np.all(got == 0.0)  # zero input -> zero expert outputs
+        # a single token and a token count that is not a multiple of the pass size
+        for n in (1, 6, 63):
+            xb = synthetic.activations(SMALL_MIX, n)
+            got, idx, _ = moe_gpu.forward(h, p, x_bits=xb, n_hash=min(n, 5))
+            ref = moe.forward(p, x_bits=xb, n_hash=min(n, 5))
+            assert np.max(np.abs(got - ref["out"])) <= moe_gpu.tolerance(ref["out"])
+    finally:
+        api.ds4moe_destroy(h)
+
+
+def test_out_of_range_token_id_sets_error_flag():
+    p = synthetic.make_problem(SMALL_MIX)
+    h = moe_gpu.create(p)
+    try:
+        bad = p.token_ids.copy()
+        bad[2] = SMALL_MIX.hash_vocab + 7
+        got, idx, w = moe_gpu.forward(h, p, token_ids=bad)
+        st = api.ds4moe_get_stats(h)
+        assert st["error_flags"] & 1
+        assert np.all(w[2] == 0)
+        assert np.all(np.isfinite(got))
+    finally:
+        api.ds4moe_destroy(h)
+
+
+def test_workspace_limit_reports_oom():
+    p = synthetic.make_problem(SMALL_MIX)
+    with pytest.raises(api.Ds4MoeError) as ei:
+        moe_gpu.create(p, workspace_limit=1 << 20)
+    assert ei.value.code == api.DS4MOE_ERR_OOM
+
+
+def test_host_entry_point_matches_device_entry_point():
+    p = synthetic.make_problem(SMALL_MIX)
+    h = moe_gpu.create(p)
+    try:
+        dev, _, _ = moe_gpu.forward(h, p)
+        out = np.zeros((SMALL_MIX.n_tokens, SMALL_MIX.d), np.float32)
+        api.ds4moe_forward_host(h, np.ascontiguousarray(p.x_bits), SMALL_MIX.n_tokens,
+                                np.ascontiguousarray(p.token_ids), SMALL_MIX.n_hash, out, 0)
+        assert np.array_equal(out.view(np.uint32), dev.view(np.uint32))
+    finally:
+        api.ds4moe_destroy(h)

@@ -148,7 +148,7 @@ def test_route_override_with_own_route_is_identity():
     ov[4] = [e for e in range(SMALL.n_experts) if e not in ref["idx"][4]][:SMALL.top_k]
     other = moe.forward(p, route_override=ov)
     rows = [t for t in range(SMALL.n_tokens) if t != 4]
-    np.testing.assert_array_equal(other["out"][rows], ref["out"][rows])
+    assert _rel_err(other["out"][rows], ref["out"][rows]) < 1e-13  # rows batched differently
     assert not np.allclose(other["out"][4], ref["out"][4])
     np.testing.assert_allclose(other["w"][4].sum(), 1.0, rtol=1e-15)
 
