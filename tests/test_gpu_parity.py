@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 MARGIN = 1e-6
 
 SMALL_MIX = synthetic.Spec("small-mix", d=512, n_experts=16, top_k=4, f=384, f_shared=256, n_shared=1,
-                           fmt_gate_up="q2_k", fmt_down="q2_k", fmt_shared="q8_0", n_tokens=37, seed=21,
+                           fmt_gate_up="q2_k", fmt_down="q8_0", fmt_shared="q8_0", n_tokens=37, seed=21,
                            bias="normal", n_hash=5, hash_vocab=100)
 SMALL_Q8_NOSHARED = synthetic.Spec("small-q8-noshared", d=384, n_experts=12, top_k=3, f=256, f_shared=128,
                                    n_shared=0, fmt_gate_up="q8_0", fmt_down="q8_0", fmt_shared="q8_0",
@@ -60,6 +60,7 @@ def check_out(p, got, ref, tokens, idx, exempt):
         want[rows] = alt[rows]
     err = np.max(np.abs(got[tokens] - want))
     tol = moe_gpu.tolerance(want)
+    print(f"parity: max err {err:.3e}, tol {tol:.3e}, ratio {err / tol:.3f}")
     assert err <= tol, f"max err {err:.3e} > tol {tol:.3e}"
     return err, tol
 
