@@ -35,7 +35,8 @@
  *
  * Shapes: routed gate/up are [f_routed x d], routed down [d x f_routed], shared gate/up
  * [f_shared x d], shared down [d x f_shared]. Every K dimension must be a multiple of 256
- * for Q2_K and of 128 for Q8_0; d, f_routed and f_shared must be multiples of 128.
+ * for Q2_K and of 128 for Q8_0; d, f_routed and f_shared must be multiples of 128, with
+ * d <= 12288 and f_routed, f_shared <= 16384.
  *
  * Error convention: every int-returning call returns DS4MOE_OK (0) or a negative code and
  * records a message readable with ds4moe_last_error() on the calling thread. Device-side

@@ -139,7 +139,8 @@ namespace {
 bool fmt_ok(int f) { return f == DS4MOE_FMT_Q8_0 || f == DS4MOE_FMT_Q2_K; }
 
 int check_shapes(const ds4moe_shapes* s) {
-  if (s->d <= 0 || s->d % 128 || s->d > 16384) return fail(DS4MOE_ERR_INVALID_ARG, "d=%d must be a positive multiple of 128 up to 16384", s->d);
+  // the router stages 8 token rows of d bf16 values in shared memory: d <= 12288 keeps that under 200 KB
+  if (s->d <= 0 || s->d % 128 || s->d > 12288) return fail(DS4MOE_ERR_INVALID_ARG, "d=%d must be a positive multiple of 128 up to 12288", s->d);
   if (s->f_routed <= 0 || s->f_routed % 128 || s->f_routed > 16384)
     return fail(DS4MOE_ERR_INVALID_ARG, "f_routed=%d must be a positive multiple of 128 up to 16384", s->f_routed);
   if (s->n_shared != 0 && s->n_shared != 1) return fail(DS4MOE_ERR_INVALID_ARG, "n_shared=%d must be 0 or 1", s->n_shared);

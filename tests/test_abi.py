@@ -48,7 +48,7 @@ def _shapes(api, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=100), -1), (dict(f_routed=0), -1), (dict(n_experts=300), -1), (dict(top_k=9, n_experts=8), -1),
+    (dict(d=100), -1), (dict(d=12800), -1), (dict(f_routed=0), -1), (dict(n_experts=300), -1), (dict(top_k=9, n_experts=8), -1),
     (dict(max_tokens=0), -1), (dict(n_shared=2), -1), (dict(fmt_gate_up=7), -2), (dict(fmt_down=-1), -2),
     (dict(d=384), -2),  # Q2_K needs K a multiple of 256
 ])
