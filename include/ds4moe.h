@@ -150,6 +150,25 @@ int ds4moe_set_profiling(ds4moe_handle* h, int32_t enable);
 int ds4moe_get_phase_times(ds4moe_handle* h, float* ms, const char** names, int32_t max_phases,
                            int32_t* n_phases);
 
+/* Routing step alone, allocating nothing (the paper has no counterpart: this is a library
+ * convenience). Some callers cannot call cudaMalloc -- an engine that carves its device memory
+ * up front and forbids later allocations, a plugin whose host owns the memory budget, a
+ * latency-critical path where cudaMalloc may synchronise the device. This call needs no handle:
+ * it computes fp32 logits of router_w (device fp32 [n_experts x d]) and router_b (device fp32
+ * [n_experts] or NULL) for x (device bf16 [n_tokens x d]), then the sigmoid top-k with ties to
+ * the lower index and weights renormalised to sum 1, into idx (device int32
+ * [n_tokens x top_k]) and w (device fp32 [n_tokens x top_k]), in top-k order -- the same
+ * kernels and results as the routing of ds4moe_forward. Runs on the calling thread's current
+ * device, asynchronously on stream. The logits live in a static device array of
+ * DS4MOE_NOALLOC_MAX_LOGITS floats that the library image carries (held by every GPU that loads
+ * the library until exit): n_tokens * n_experts above that returns DS4MOE_ERR_CAPACITY. The
+ * first call on a device looks the array's address up (cudaGetSymbolAddress); make it before
+ * any stream capture. All calls on a device share the array, so calls that may overlap on the
+ * GPU (unordered streams) race. */
+#define DS4MOE_NOALLOC_MAX_LOGITS 262144
+int ds4moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int32_t n_tokens,
+                         int32_t d, int32_t n_experts, int32_t top_k, int32_t* idx, float* w, void* stream);
+
 /* Frees everything the handle owns. NULL is allowed. Synchronises the device first. */
 void ds4moe_destroy(ds4moe_handle* h);
 

@@ -59,6 +59,11 @@ PtrKind classify(const void* p, int device) {
 
 }  // namespace
 
+namespace ds4 {
+// Lets the other translation units report errors through ds4moe_last_error.
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace ds4
+
 struct ds4moe_handle {
   ds4moe_shapes s{};
   int64_t bytes = 0;

@@ -30,8 +30,9 @@ FORMATS = {"q8_0": DS4MOE_FMT_Q8_0, "q2_k": DS4MOE_FMT_Q2_K}
 
 EXPORTED = ("ds4moe_create", "ds4moe_forward", "ds4moe_forward_ex", "ds4moe_forward_host",
             "ds4moe_get_route", "ds4moe_get_stats", "ds4moe_device_bytes",
-            "ds4moe_launches_per_forward", "ds4moe_set_profiling", "ds4moe_get_phase_times", "ds4moe_destroy",
-            "ds4moe_last_error")
+            "ds4moe_launches_per_forward", "ds4moe_set_profiling", "ds4moe_get_phase_times", "ds4moe_route_noalloc",
+            "ds4moe_destroy", "ds4moe_last_error")
+DS4MOE_NOALLOC_MAX_LOGITS = 262144
 
 
 class ds4moe_shapes(ctypes.Structure):
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_get_phase_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), i32,
                                              ctypes.POINTER(i32)]
         L.ds4moe_get_phase_times.restype = ctypes.c_int
+        L.ds4moe_route_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        L.ds4moe_route_noalloc.restype = ctypes.c_int
         L.ds4moe_destroy.argtypes = [vp]
         L.ds4moe_destroy.restype = None
         L.ds4moe_last_error.argtypes = []
@@ -186,6 +189,13 @@ def ds4moe_get_phase_times(h: int) -> list:
     n = ctypes.c_int32()
     _check(lib().ds4moe_get_phase_times(h, ms, names, cap, ctypes.byref(n)))
     return [(names[i].decode(), float(ms[i])) for i in range(min(n.value, cap))]
+
+
+def ds4moe_route_noalloc(router_w, router_b, x, n_tokens: int, d: int, n_experts: int, top_k: int, idx, w,
+                         stream: int = 0) -> None:
+    """Routing without any device allocation (for callers that cannot allocate); see the header."""
+    _check(lib().ds4moe_route_noalloc(_ptr(router_w), _ptr(router_b), _ptr(x), n_tokens, d, n_experts, top_k,
+                                      _ptr(idx), _ptr(w), stream))
 
 
 def ds4moe_destroy(h: Optional[int]) -> None:
