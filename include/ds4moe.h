@@ -91,7 +91,8 @@ typedef struct ds4moe_weights {
     const void* shared_gate;    /* [f_shared x d], NULL when n_shared == 0 */
     const void* shared_up;      /* [f_shared x d] */
     const void* shared_down;    /* [d x f_shared] */
-    const int32_t* hash_table;  /* int32 [hash_vocab x top_k], distinct ids per row; NULL if none */
+    const int32_t* hash_table;  /* int32 [hash_vocab x top_k], distinct ids in [0, E) per row (checked
+                                   at create: DS4MOE_ERR_INVALID_ARG otherwise); NULL if none */
 } ds4moe_weights;
 
 typedef struct ds4moe_stats {

@@ -139,6 +139,55 @@ struct GemvArgs {
   float* out;               // gate/up: H [pos x rows]; down: Y [pos x rows]
 };
 
+// Everything the three decode kernels read and write (device pointers).
+struct DecodeArgs {
+  const __nv_bfloat16* x;
+  int n_tok, d;
+  const float* wr;
+  const float* br;
+  int n_exp, top_k;
+  const int* token_ids;
+  int n_hash;
+  const int* table;
+  int vocab;
+  float* logits;      // [n_learned x E]
+  float* xmax;        // [n_tok] max |x| per token
+  int* idx;           // [n_tok x top_k]
+  float* wts;
+  int* counts;        // [E]
+  int* offsets;       // [E+1]
+  int* active;        // [E]
+  int* n_active;
+  int* perm;          // [n_tok x top_k]
+  int* rowof;
+  int* err;
+  unsigned int* counter;  // arrival counter of the route kernel, zero between forwards
+  float* hmax;        // [n_tok x top_k + n_tok] max |h| per routed slot position, then per token
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  size_t mb_gu, mb_d;
+  int f;
+  const uint8_t* sgate;
+  const uint8_t* sup;
+  const uint8_t* sdown;
+  size_t mb_sgu, mb_sd;
+  int fs, n_shared;
+  float* H;           // [n_tok x top_k x f] by bucketed position
+  float* Hs;          // [n_tok x fs]
+  float* out;         // [n_tok x d]
+};
+
+// Optional callback after each launch (per-launch timing).
+struct DecodeHooks {
+  void (*mark)(void* ctx, const char* name);
+  void* ctx;
+};
+
+int decode_max_tokens();
+cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
+                          int* launches, const DecodeHooks* hooks);
+
 void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s);
 void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float* w, const float* b, int n_exp,
                           float* logits, cudaStream_t s);

@@ -94,6 +94,9 @@ struct ds4moe_handle {
   float* Y = nullptr;
   float* Ys = nullptr;
   int* err = nullptr;
+  float* xmax = nullptr;
+  float* hmax = nullptr;
+  unsigned int* counter = nullptr;
   // host-call staging
   __nv_bfloat16* x_stage = nullptr;
   int* tid_stage = nullptr;
@@ -223,6 +226,16 @@ int repack_stack(ds4moe_handle* h, int fmt, const void* src, uint8_t* dst, int n
   return rc;
 }
 
+// Every table entry must name a routed expert: the bucketing indexes per-expert arrays by it.
+int check_table(const int* dev_table, size_t n, int n_exp) {
+  std::vector<int> host(n);
+  DS4_CUDA(cudaMemcpy(host.data(), dev_table, n * 4, cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < n; ++i)
+    if (host[i] < 0 || host[i] >= n_exp)
+      return fail(DS4MOE_ERR_INVALID_ARG, "hash_table entry %zu is %d, outside [0, n_experts=%d)", i, host[i], n_exp);
+  return DS4MOE_OK;
+}
+
 #define DS4_TRY(call)          \
   do {                         \
     int rc_ = (call);          \
@@ -282,6 +295,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   if (s->hash_vocab > 0) {
     DS4_TRY(h->alloc_t(&h->table, (size_t)s->hash_vocab * K * 4));
     DS4_TRY(copy_in(h->table, w->hash_table, (size_t)s->hash_vocab * K * 4, s->device, "hash_table"));
+    DS4_TRY(check_table(h->table, (size_t)s->hash_vocab * K, E));
   }
   // workspace for max_tokens
   const size_t M = (size_t)s->max_tokens, slots = M * K;
@@ -301,12 +315,16 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
     DS4_TRY(h->alloc_t(&h->Ys, M * d * 4));
   }
   DS4_TRY(h->alloc_t(&h->err, 4));
+  DS4_TRY(h->alloc_t(&h->xmax, M * 4));
+  DS4_TRY(h->alloc_t(&h->hmax, (slots + M) * 4));
+  DS4_TRY(h->alloc_t(&h->counter, 4));
   DS4_TRY(h->alloc_t(&h->x_stage, M * d * 2));
   DS4_TRY(h->alloc_t(&h->tid_stage, M * 4));
   DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
   cudaError_t e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->counter, 0, 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     rc = fail(DS4MOE_ERR_CUDA, "workspace init: %s", cudaGetErrorString(e));
@@ -353,6 +371,29 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
       cudaEventRecord(h->ev[++phase], st);
     }
   };
+  if (n <= ds4::decode_max_tokens()) {
+    // decode path: three kernels, chained with programmatic dependent launch unless profiling
+    ds4::DecodeArgs da{};
+    da.x = xb; da.n_tok = n; da.d = d; da.wr = h->router_w; da.br = h->router_b; da.n_exp = E; da.top_k = K;
+    da.token_ids = token_ids; da.n_hash = n_hash; da.table = h->table; da.vocab = s.hash_vocab;
+    da.logits = h->logits; da.xmax = h->xmax; da.idx = h->idx; da.wts = h->wts; da.counts = h->counts;
+    da.offsets = h->offsets; da.active = h->active; da.n_active = h->n_active; da.perm = h->perm;
+    da.rowof = h->rowof; da.err = h->err; da.counter = h->counter; da.hmax = h->hmax;
+    da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = f;
+    da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
+    da.fs = fs; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
+    struct Ctx {
+      decltype(mark)* m;
+    } ctx{&mark};
+    ds4::DecodeHooks hooks{[](void* c, const char* name) { (*static_cast<Ctx*>(c)->m)(name); }, &ctx};
+    cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, !h->profile, st, nullptr,
+                                       h->profile ? &hooks : nullptr);
+    if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    h->n_phases = phase;
+    h->last_stream = st;
+    h->last_n = n;
+    return DS4MOE_OK;
+  }
   if (n_learned > 0) {
     ds4::launch_router_logits(xb + (size_t)n_hash * d, n_learned, d, h->router_w, h->router_b, E, h->logits, st);
     mark("router_logits");
@@ -447,6 +488,7 @@ extern "C" int64_t ds4moe_device_bytes(const ds4moe_handle* h) { return h ? h->b
 
 extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n_tokens) {
   if (!h || n_tokens <= 0) return 0;
+  if (n_tokens <= ds4::decode_max_tokens()) return 3;  // route, gate/up, down + combine
   // router, top-k, 2 bucketing, gate/up + down routed, the same for shared, combine
   return 1 + 1 + 2 + 2 + (h->s.n_shared ? 2 : 0) + 1;
 }

@@ -111,3 +111,12 @@ def test_host_entry_point_matches_device_entry_point():
         assert np.array_equal(out.view(np.uint32), dev.view(np.uint32))
     finally:
         api.ds4moe_destroy(h)
+
+
+def test_table_entries_outside_the_expert_range_are_refused():
+    p = synthetic.make_problem(SMALL_MIX)
+    bad = p.hash_table.copy()
+    bad[7, 1] = SMALL_MIX.n_experts
+    with pytest.raises(api.Ds4MoeError) as ei:
+        moe_gpu.create(dataclasses.replace(p, hash_table=bad))
+    assert ei.value.code == api.DS4MOE_ERR_INVALID_ARG
