@@ -14,7 +14,8 @@ from test_gpu_parity import SMALL_MIX
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("spec,reps", [(synthetic.CONFIGS[1], 20), (SMALL_MIX, 20), (synthetic.CONFIGS[3], 5)],
+@pytest.mark.parametrize("spec,reps", [(synthetic.CONFIGS[1], 20), (synthetic.CONFIGS[2], 10), (SMALL_MIX, 20),
+                                       (synthetic.CONFIGS[3], 5)],
                          ids=lambda v: getattr(v, "name", str(v)))
 def test_repeated_forwards_are_bitwise_identical(spec, reps):
     p = synthetic.make_problem(spec)
@@ -69,7 +70,7 @@ def test_token_count_edges():
         assert all(sorted(r) == sorted(want.tolist()) for r in idx.tolist())
         assert np.all(got == 0.0)  # zero input -> zero expert outputs
         # a single token and a token count that is not a multiple of the pass size
-        for n in (1, 6, 63):
+        for n in (1, 6, 16, 17, 63):  # decode path up to 16 tokens, the batched path above
             xb = synthetic.activations(SMALL_MIX, n)
             got, idx, _ = moe_gpu.forward(h, p, x_bits=xb, n_hash=min(n, 5))
             ref = moe.forward(p, x_bits=xb, n_hash=min(n, 5))
