@@ -316,9 +316,11 @@ __global__ void __launch_bounds__(kThreads) gateup_decode_kernel(DecodeArgs a, i
           if (t == 0) red[warp][m][tt][g + 8 * rho] = v;
         }
     __syncthreads();
-    if (threadIdx.x < 16 * kPass) {  // warps 0 and 1 take part whole (the shuffles below)
-      const int tt = threadIdx.x >> 4, r = threadIdx.x & 15;
-      const bool valid = tt < np;
+    // whole warps take part (the 16-lane shuffles below name all 32 lanes): warp 0 for one
+    // token per pass, warps 0 and 1 for four
+    if (threadIdx.x < (kPass == 1 ? 32 : 16 * kPass)) {
+      const int tt = min(threadIdx.x >> 4, kPass - 1), r = threadIdx.x & 15;
+      const bool valid = (int)(threadIdx.x >> 4) < np;
       float s0 = 0.f, s1 = 0.f;
       for (int w = 0; w < kWarps; ++w) {
         s0 += red[w][0][tt][r];
