@@ -158,16 +158,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
 
+def oracle_token(problem, spec, xb, n):
+    """fp64 oracle forward of token n of the batch xb (table-routed when n < n_hash)."""
+    from oracle import moe
+    nh = 1 if n < spec.n_hash else 0
+    tid = problem.token_ids[n:n + 1] if nh else None
+    return moe.forward(problem, x_bits=xb[n:n + 1], token_ids=tid, n_hash=nh)
+
+
 def oracle_sample(spec, problem, seconds: float, min_tokens: int = 1):
     """Runs the fp64 oracle on successive tokens of the workload until `seconds` elapse."""
-    from oracle import moe
-    x = problem.x_bits
+    xb = synthetic.activations(spec, max(spec.n_tokens, 256))
     n = 0
     t0 = time.perf_counter()
     while n < min_tokens or time.perf_counter() - t0 < seconds:
-        if n >= x.shape[0]:
+        if n >= xb.shape[0]:
             break
-        moe.forward(problem, tokens=[n])
+        oracle_token(problem, spec, xb, n)
         n += 1
     dt = time.perf_counter() - t0
     return n, dt
@@ -177,13 +184,13 @@ def run_reference(args, spec, rank):
     if rank != 0:
         return
     problem = synthetic.make_problem(spec)
+    xb = synthetic.activations(spec, max(spec.n_tokens, 256))
     # one step = one token of the workload through the oracle (bounded sample)
-    from oracle import moe
     tok = 0
 
     def step():
         nonlocal tok
-        moe.forward(problem, tokens=[tok % spec.n_tokens])
+        oracle_token(problem, spec, xb, tok % xb.shape[0])
         tok += 1
 
     for _ in range(args.warmup):
@@ -272,11 +279,8 @@ def main():
     torch.cuda.synchronize()
 
     # timed region: each step timed alone with events on the launching stream, L2 flushed between
-    api.ds4moe_set_profiling(h, True)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    phase_ms: dict[str, list] = {}
-    distinct = []
     sampler = ClockSampler(local) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -288,14 +292,10 @@ def main():
         starts[i].record(stream)
         fwd(i)
         ends[i].record(stream)
-        for name, ms in api.ds4moe_get_phase_times(h):  # waits for this step
-            phase_ms.setdefault(name, []).append(ms)
-        distinct.append(api.ds4moe_get_stats(h)["distinct_experts"])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    api.ds4moe_set_profiling(h, False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = float(sum(step_ms))
     if world > 1:
@@ -305,6 +305,19 @@ def main():
     tokens = world * spec.n_tokens * args.steps
     value = tokens / (total_ms / 1e3)
     ms_per_step = total_ms / args.steps
+
+    # per-launch times of the same workload: events recorded between the launches (this
+    # serialises the launches, so it runs after the timed region, over the same inputs)
+    api.ds4moe_set_profiling(h, True)
+    phase_ms: dict[str, list] = {}
+    distinct = []
+    for i in range(args.steps):
+        flush_buf.zero_()
+        fwd(i)
+        for name, ms in api.ds4moe_get_phase_times(h):  # waits for this step
+            phase_ms.setdefault(name, []).append(ms)
+        distinct.append(api.ds4moe_get_stats(h)["distinct_experts"])
+    api.ds4moe_set_profiling(h, False)
 
     # end to end through the host entry point: pinned host input, copies inside the timed region
     x_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.int16, pin_memory=True)
@@ -343,7 +356,11 @@ def main():
     flops = forward_flops(spec)
     bytes_alg = {"routed_gateup": wb["routed_gateup"] + wb["x"], "routed_down": wb["routed_down"],
                  "shared_gateup": wb["shared"] * 2 / 3 + wb["x"], "shared_down": wb["shared"] / 3,
-                 "router_logits": wb["router"] + wb["x"], "combine": wb["out"]}
+                 "router_logits": wb["router"] + wb["x"], "combine": wb["out"],
+                 # decode path: gate/up of the touched and the shared experts; down + combine
+                 "route": wb["router"] + wb["x"],
+                 "gateup": wb["routed_gateup"] + wb["shared"] * 2 / 3 + wb["x"],
+                 "down_combine": wb["routed_down"] + wb["shared"] / 3 + wb["out"]}
     decode = spec.n_tokens <= 64
     if decode:
         achieved = bytes_alg.get(top, 0.0) / (mean_phase[top] / 1e3) / 1e9
