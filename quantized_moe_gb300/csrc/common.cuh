@@ -160,6 +160,9 @@ struct DecodeArgs {
   int* n_active;
   int* perm;          // [n_tok x top_k]
   int* rowof;
+  int4* work;         // [E] per active expert: expert id, first bucketed position, count (0 past n_active)
+  int* tokof;         // [n_tok x top_k] token of each bucketed position
+  float* xscale;      // [n_tok] power-of-two fp16 scale of each token
   int* err;
   unsigned int* counter;  // arrival counter of the route kernel, zero between forwards
   float* hmax;        // [n_tok x top_k + n_tok] max |h| per routed slot position, then per token
@@ -185,6 +188,7 @@ struct DecodeHooks {
 };
 
 int decode_max_tokens();
+int decode_max_slots();
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks);
 

@@ -1,19 +1,23 @@
-// Decode path (1..16 tokens): three kernels chained with programmatic dependent launch.
+// Decode path (1..16 tokens, at most 128 routed slots): three kernels chained with
+// programmatic dependent launch.
 //
 //  route_decode_kernel    one CTA per routed expert computes its fp32 logits for every token;
 //                         the last CTA to finish (atomic arrival counter, no waiting) runs the
-//                         sigmoid top-k (or table routing), the bucketing and the bookkeeping.
-//                         CTA 0 also records max|x| per token for the fp16 activation scale.
-//  gateup_decode_kernel   CTA = 16 rows of f of one active expert (or of the shared expert),
-//                         K split over 8 warps; h = silu(g) * u written in fp32, and max|h| per
-//                         row of H reduced with an integer atomicMax (order-free).
-//  down_decode_kernel     CTA = 16 rows of d for ALL touched experts and the shared expert; the
-//                         per-slot results stay in shared memory and the CTA writes the final
-//                         out rows: routed terms in ascending expert id, then the shared expert.
+//                         sigmoid top-k (or table routing), the bucketing, and publishes a work
+//                         list (expert, first position, count) per active expert, the token of
+//                         every bucketed position and the fp16 scale of every token.
+//  gateup_decode_kernel   CTA = 16 rows of f of one active expert (or of the shared expert), K
+//                         split over 8 warps, each warp streaming its units through a two-deep
+//                         register pipeline; h = silu(g) * u in fp32 plus max|h| per row of H
+//                         (integer atomicMax: order-free).
+//  down_decode_kernel     CTA = 16 rows of d for every touched expert and the shared expert;
+//                         (expert, K unit) items are dealt round-robin to the warps, each warp
+//                         accumulates its partials in shared memory in a fixed order, and the
+//                         CTA writes the final rows: routed terms in ascending expert id, then
+//                         the shared expert.
 //
-// Before waiting on its predecessor, each dependent kernel streams the weights that do not
-// depend on the routing (and, for the down kernel, the routed weights, whose routing is final
-// by then) into L2, so weight reads overlap the previous kernel.
+// Weights that do not depend on the previous kernel's output are loaded before waiting on it:
+// the shared expert's gate/up units, and (the routing being final by then) every down unit.
 #include "mma_units.cuh"
 
 namespace ds4 {
@@ -21,7 +25,9 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 256;
-constexpr int kMaxTok = 16;  // decode path limit
+constexpr int kMaxTok = 16;
+constexpr int kMaxSlots = 128;
+constexpr int kMaxJ = 12;  // d <= 12288: float4 loads per lane of one router row slice
 
 // ----------------------------------------------------------------------------- route
 
@@ -29,37 +35,40 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   __shared__ float part[kWarps][kMaxTok];
   __shared__ float xmx[kWarps][kMaxTok];
   __shared__ int s_last;
-  __shared__ int s_idx[kMaxTok * 16];
+  __shared__ int s_idx[kMaxSlots];
   __shared__ int s_cnt[256], s_off[257], s_act[256], s_nact;
   const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, nt = a.n_tok;
-  // ---- logits of expert e for the learned tokens (and max|x| of every token in CTA 0)
-  const int per_warp = d / kWarps;
-  const float* wr = a.wr + (size_t)e * d;
-  float acc[kMaxTok], mx[kMaxTok];
+  // ---- logits of expert e for the learned tokens (and max|x| of every token in CTA 0);
+  // each lane first issues all its loads of the router row slice
+  // lane covers k = warp * per_warp + 4 lane + 128 j (per_warp is a multiple of 16)
+  const int per_warp = d / kWarps, nj = per_warp > 4 * lane ? (per_warp - 4 * lane + 127) / 128 : 0;
+  const float* wr = a.wr + (size_t)e * d + warp * per_warp + lane * 4;
+  float4 wv[kMaxJ];
 #pragma unroll
-  for (int t = 0; t < kMaxTok; ++t) acc[t] = mx[t] = 0.f;
-  for (int k0 = warp * per_warp + lane * 4; k0 < (warp + 1) * per_warp; k0 += 128) {
-    const float4 wv = *reinterpret_cast<const float4*>(wr + k0);
+  for (int j = 0; j < kMaxJ; ++j)
+    if (j < nj) wv[j] = *reinterpret_cast<const float4*>(wr + 128 * j);
+  for (int t = 0; t < nt; ++t) {
+    const __nv_bfloat16* xr = a.x + (size_t)t * d + warp * per_warp + lane * 4;
+    uint2 xv[kMaxJ];
 #pragma unroll
-    for (int t = 0; t < kMaxTok; ++t) {
-      if (t >= nt) break;
-      const uint2 xv = *reinterpret_cast<const uint2*>(a.x + (size_t)t * d + k0);
-      const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
-      const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
-      acc[t] = fmaf(wv.x, x01.x, acc[t]);
-      acc[t] = fmaf(wv.y, x01.y, acc[t]);
-      acc[t] = fmaf(wv.z, x23.x, acc[t]);
-      acc[t] = fmaf(wv.w, x23.y, acc[t]);
-      mx[t] = fmaxf(mx[t], fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y))));
+    for (int j = 0; j < kMaxJ; ++j)
+      if (j < nj) xv[j] = *reinterpret_cast<const uint2*>(xr + 128 * j);
+    float acc = 0.f, mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxJ; ++j) {
+      if (j >= nj) break;
+      const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv[j].x));
+      const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv[j].y));
+      acc = fmaf(wv[j].x, x01.x, acc);
+      acc = fmaf(wv[j].y, x01.y, acc);
+      acc = fmaf(wv[j].z, x23.x, acc);
+      acc = fmaf(wv[j].w, x23.y, acc);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y))));
     }
-  }
-#pragma unroll
-  for (int t = 0; t < kMaxTok; ++t) {
-    if (t >= nt) break;
-    const float s = warp_sum(acc[t]);
-    const float m = warp_max(mx[t]);
-    if (lane == 0) { part[warp][t] = s; xmx[warp][t] = m; }
+    acc = warp_sum(acc);
+    mx = warp_max(mx);
+    if (lane == 0) { part[warp][t] = acc; xmx[warp][t] = mx; }
   }
   __syncthreads();
   if (threadIdx.x < nt) {
@@ -160,7 +169,16 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   for (int i = threadIdx.x; i < E; i += kThreads) {
     a.counts[i] = s_cnt[i];
     a.offsets[i] = s_off[i];
-    if (i < s_nact) a.active[i] = s_act[i];
+  }
+  const int max_active = min(E, n_slots);
+  for (int i = threadIdx.x; i < max_active; i += kThreads) {  // the work list, empty past n_active
+    int4 w = make_int4(0, 0, 0, 0);
+    if (i < s_nact) {
+      const int ex = s_act[i];
+      w = make_int4(ex, s_off[ex], s_cnt[ex], 0);
+      a.active[i] = ex;
+    }
+    a.work[i] = w;
   }
   if (threadIdx.x == 0) {
     a.offsets[E] = s_off[E];
@@ -173,357 +191,429 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
     const int pos = s_off[ex] + r;
     a.perm[pos] = sl;
     a.rowof[sl] = pos;
+    a.tokof[pos] = sl / K;
   }
+  for (int t = threadIdx.x; t < nt; t += kThreads) a.xscale[t] = fp16_row_scale(__ldcg(a.xmax + t));
   for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
   if (threadIdx.x == 0) *a.counter = 0u;  // every CTA has arrived: ready for the next forward
 }
 
+// ----------------------------------------------------------------------------- unit pipelines
+
+template <int FMT>
+struct Unit;
+template <>
+struct Unit<FMT_Q2_K> {
+  Q2kUnitRegs r;
+  __device__ __forceinline__ void load(const uint8_t* p) { r = q2k_load(p); }
+  static constexpr int kChunks = 2;
+};
+template <>
+struct Unit<FMT_Q8_0> {
+  Q80UnitRegs r;
+  __device__ __forceinline__ void load(const uint8_t* p) { r = q80_load(p); }
+  static constexpr int kChunks = 1;
+};
+
+// Accumulates one unit of one matrix for np token fragments; acc[tt][rho] is the lane partial of
+// row g + 8 rho (scaled by the token's fp16 scale).
+template <int P>
+__device__ __forceinline__ void unit_mma(const Unit<FMT_Q2_K>& u, const XFrag (&xf)[P][2], int np, const BMask& bm,
+                                         const Q2kLaneConst& qc, float (&acc)[P][2]) {
+  float as[P][2], am[P][2];
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) as[tt][0] = as[tt][1] = am[tt][0] = am[tt][1] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t w[4] = {u.r.q[c].x, u.r.q[c].y, u.r.q[c].z, u.r.q[c].w};
+    const uint32_t wh[4] = {w[0] >> 10, w[1] >> 10, w[2] >> 10, w[3] >> 10};
+    const Q2kChunkScales s = q2k_chunk_scales(u.r.sc[c], qc);
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) {
+      if (tt >= np) break;
+      float dd[4];
+      q2k_chunk_mma(w, wh, bm, xf[tt][c], dd);
+      as[tt][0] = fmaf(s.s00, dd[0], fmaf(s.s01, dd[1], as[tt][0]));
+      as[tt][1] = fmaf(s.s10, dd[2], fmaf(s.s11, dd[3], as[tt][1]));
+      am[tt][0] = fmaf(s.m00, xf[tt][c].s0, fmaf(s.m01, xf[tt][c].s1, am[tt][0]));
+      am[tt][1] = fmaf(s.m10, xf[tt][c].s0, fmaf(s.m11, xf[tt][c].s1, am[tt][1]));
+    }
+  }
+  const float2 d0 = __half22float2(*reinterpret_cast<const __half2*>(&u.r.dd0));
+  const float2 d1 = __half22float2(*reinterpret_cast<const __half2*>(&u.r.dd1));
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) {
+    if (tt >= np) break;
+    acc[tt][0] = fmaf(d0.x, as[tt][0], fmaf(-d0.y, am[tt][0], acc[tt][0]));
+    acc[tt][1] = fmaf(d1.x, as[tt][1], fmaf(-d1.y, am[tt][1], acc[tt][1]));
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void unit_mma(const Unit<FMT_Q8_0>& u, const XFrag (&xf)[P][2], int np, const BMask& bm,
+                                         const Q2kLaneConst&, float (&acc)[P][2]) {
+  const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&u.r.sc));
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) {
+    if (tt >= np) break;
+    float dd[4];
+    q80_chunk_mma(u.r.v, bm, xf[tt][0], dd);
+    const float off = 128.f * (xf[tt][0].s0 + xf[tt][0].s1);
+    acc[tt][0] = fmaf(s.x, fmaf(16777216.f, dd[0] + dd[1], -off), acc[tt][0]);
+    acc[tt][1] = fmaf(s.y, fmaf(16777216.f, dd[2] + dd[3], -off), acc[tt][1]);
+  }
+}
+
 // ----------------------------------------------------------------------------- gate/up
 
-// kPass: token rows per pass through the weights (1 for a single token, else 4)
-template <int FMT_R, int FMT_S, int kPass>
-__global__ void __launch_bounds__(kThreads) gateup_decode_kernel(DecodeArgs a, int max_active) {
-  __shared__ float red[kWarps][2][kPass][16];
-  const int rg = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const bool shared = (int)blockIdx.y == max_active;
-  const int d = a.d;
-  const int rows = shared ? a.fs : a.f;
-  if (rg * 16 >= rows) {
-    pdl_wait();
-    return;
+// One pipeline stage of the gate/up kernel: the gate and up units of one K unit plus the raw
+// activation words of the pass's tokens for its chunks.
+template <int FMT, int P>
+struct GuStage {
+  Unit<FMT> g, u;
+  uint2 xr[P][2];
+};
+
+template <int FMT, int P>
+__device__ __forceinline__ void gu_load_w(GuStage<FMT, P>& st, const uint8_t* w0, const uint8_t* w1, int rg, int kb,
+                                          int n_kb) {
+  st.g.load(w0 + unit_offset(rg, kb, n_kb, unit_bytes(FMT)));
+  st.u.load(w1 + unit_offset(rg, kb, n_kb, unit_bytes(FMT)));
+}
+
+template <int FMT, int P>
+__device__ __forceinline__ void gu_load_x(GuStage<FMT, P>& st, const __nv_bfloat16* const (&xrow)[P], int np, int kb) {
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) {
+    if (tt >= np) break;
+#pragma unroll
+    for (int c = 0; c < Unit<FMT>::kChunks; ++c) st.xr[tt][c] = xraw_bf16(xrow[tt] + kb * unit_k(FMT) + 128 * c);
   }
-  const int fmt = shared ? FMT_S : FMT_R;
-  const int n_kb = d / unit_k(fmt);
-  const int ub = unit_bytes(fmt);
-  const uint8_t* w0 = shared ? a.sgate : a.gate;
-  const uint8_t* w1 = shared ? a.sup : a.up;
-  const size_t mb = shared ? a.mb_sgu : a.mb_gu;
-  if (shared) {  // routing-independent weights: start their reads before the router finishes
-    for (int kb = warp; kb < n_kb; kb += kWarps) {
-      prefetch_l2(w0 + unit_offset(rg, kb, n_kb, ub), ub);
-      prefetch_l2(w1 + unit_offset(rg, kb, n_kb, ub), ub);
+}
+
+template <int FMT, int P>
+__device__ __forceinline__ void gu_compute(const GuStage<FMT, P>& st, const float (&sc)[P], int np, const BMask& bm,
+                                           const Q2kLaneConst& qc, float (&accg)[P][2], float (&accu)[P][2]) {
+  XFrag xf[P][2];
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) {
+    if (tt >= np) break;
+#pragma unroll
+    for (int c = 0; c < Unit<FMT>::kChunks; ++c) xf[tt][c] = xfrag_from_bf16(st.xr[tt][c], sc[tt]);
+  }
+  unit_mma<P>(st.g, xf, np, bm, qc, accg);
+  unit_mma<P>(st.u, xf, np, bm, qc, accu);
+}
+
+// The K units kb = warp + 8 i of one CTA row group, through a two-deep register pipeline.
+// The first two stages may already hold their weights (loaded before the dependency wait).
+template <int FMT, int P>
+__device__ __forceinline__ void gu_stream(GuStage<FMT, P>& s0, GuStage<FMT, P>& s1, bool preloaded,
+                                          const uint8_t* w0, const uint8_t* w1, int rg, int n_kb,
+                                          const __nv_bfloat16* const (&xrow)[P], const float (&sc)[P], int np,
+                                          const BMask& bm, const Q2kLaneConst& qc, float (&accg)[P][2],
+                                          float (&accu)[P][2]) {
+  const int warp = threadIdx.x >> 5;
+  const int nk = n_kb > warp ? (n_kb - warp + kWarps - 1) / kWarps : 0;
+  if (!preloaded) {
+    if (nk > 0) gu_load_w(s0, w0, w1, rg, warp, n_kb);
+    if (nk > 1) gu_load_w(s1, w0, w1, rg, warp + kWarps, n_kb);
+  }
+  if (nk > 0) gu_load_x(s0, xrow, np, warp);
+  if (nk > 1) gu_load_x(s1, xrow, np, warp + kWarps);
+  for (int i = 0; i < nk; i += 2) {
+    gu_compute(s0, sc, np, bm, qc, accg, accu);
+    if (i + 2 < nk) {
+      gu_load_w(s0, w0, w1, rg, warp + kWarps * (i + 2), n_kb);
+      gu_load_x(s0, xrow, np, warp + kWarps * (i + 2));
+    }
+    if (i + 1 < nk) {
+      gu_compute(s1, sc, np, bm, qc, accg, accu);
+      if (i + 3 < nk) {
+        gu_load_w(s1, w0, w1, rg, warp + kWarps * (i + 3), n_kb);
+        gu_load_x(s1, xrow, np, warp + kWarps * (i + 3));
+      }
     }
   }
-  pdl_wait();
-  pdl_trigger();
-  int pos0 = 0, cnt = a.n_tok;
-  if (!shared) {
-    if ((int)blockIdx.y >= *a.n_active) return;
-    const int e = a.active[blockIdx.y];
-    pos0 = a.offsets[e];
-    cnt = a.offsets[e + 1] - pos0;
-    w0 += (size_t)e * mb;
-    w1 += (size_t)e * mb;
+}
+
+// Quad and warp reductions of one pass, SwiGLU, store of h and of max|h| per row.
+template <int P>
+__device__ __forceinline__ void gu_epilogue(float (&red)[kWarps][2][P][16], const float (&accg)[P][2],
+                                            const float (&accu)[P][2], const float (&sc)[P], int np, float* hbase,
+                                            int ldh, int row0, int rg, float* hmax_row0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt)
+#pragma unroll
+    for (int rho = 0; rho < 2; ++rho) {
+      float vg = accg[tt][rho], vu = accu[tt][rho];
+      vg += __shfl_xor_sync(0xffffffffu, vg, 1);
+      vg += __shfl_xor_sync(0xffffffffu, vg, 2);
+      vu += __shfl_xor_sync(0xffffffffu, vu, 1);
+      vu += __shfl_xor_sync(0xffffffffu, vu, 2);
+      if (t == 0) { red[warp][0][tt][g + 8 * rho] = vg; red[warp][1][tt][g + 8 * rho] = vu; }
+    }
+  __syncthreads();
+  if (threadIdx.x < (P == 1 ? 32 : 16 * P)) {  // whole warps: the 16-lane shuffles below name all 32
+    const int tt = min((int)threadIdx.x >> 4, P - 1), r = threadIdx.x & 15;
+    const bool valid = (int)(threadIdx.x >> 4) < np;
+    float sg = 0.f, su = 0.f;
+    for (int w = 0; w < kWarps; ++w) { sg += red[w][0][tt][r]; su += red[w][1][tt][r]; }
+    const float inv = 1.f / sc[tt];
+    const float h = valid ? silu_mul(sg * inv, su * inv) : 0.f;
+    if (valid) hbase[(size_t)(row0 + tt) * ldh + rg * 16 + r] = h;
+    float m = fabsf(h);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, 16));
+    if (valid && r == 0) atomicMax(reinterpret_cast<unsigned*>(hmax_row0 + tt), __float_as_uint(m));
   }
+  __syncthreads();
+}
+
+template <int FMT_R, int FMT_S, int P>
+__global__ void __launch_bounds__(kThreads) gateup_decode_kernel(DecodeArgs a, int max_active) {
+  __shared__ float red[kWarps][2][P][16];
+  const int rg = blockIdx.x, warp = threadIdx.x >> 5;
+  const bool shared = (int)blockIdx.y == max_active;
   const BMask bm;
   const Q2kLaneConst qc;
-  for (int p0 = 0; p0 < cnt; p0 += kPass) {
-    const int np = min(kPass, cnt - p0);
-    const __nv_bfloat16* xrow[kPass];
-    float sc[kPass];
+  if (shared) {
+    if (rg * 16 >= a.fs) return;
+    const int n_kb = a.d / unit_k(FMT_S);
+    GuStage<FMT_S, P> s0, s1;
+    const int nk = n_kb > warp ? (n_kb - warp + kWarps - 1) / kWarps : 0;
+    // the shared expert does not depend on the routing: load its first units right away
+    if (nk > 0) gu_load_w(s0, a.sgate, a.sup, rg, warp, n_kb);
+    if (nk > 1) gu_load_w(s1, a.sgate, a.sup, rg, warp + kWarps, n_kb);
+    pdl_wait();
+    pdl_trigger();
+    for (int p0 = 0; p0 < a.n_tok; p0 += P) {
+      const int np = min(P, a.n_tok - p0);
+      const __nv_bfloat16* xrow[P];
+      float sc[P];
 #pragma unroll
-    for (int tt = 0; tt < kPass; ++tt) {
-      const int pos = pos0 + p0 + min(tt, np - 1);
-      const int tok = shared ? pos : a.perm[pos] / a.top_k;
-      xrow[tt] = a.x + (size_t)tok * d;
-      sc[tt] = fp16_row_scale(a.xmax[tok]);
+      for (int tt = 0; tt < P; ++tt) {
+        const int tok = p0 + min(tt, np - 1);
+        xrow[tt] = a.x + (size_t)tok * a.d;
+        sc[tt] = a.xscale[tok];
+      }
+      float accg[P][2], accu[P][2];
+#pragma unroll
+      for (int tt = 0; tt < P; ++tt) accg[tt][0] = accg[tt][1] = accu[tt][0] = accu[tt][1] = 0.f;
+      gu_stream<FMT_S, P>(s0, s1, p0 == 0, a.sgate, a.sup, rg, n_kb, xrow, sc, np, bm, qc, accg, accu);
+      gu_epilogue<P>(red, accg, accu, sc, np, a.Hs, a.fs, p0, rg, a.hmax + a.n_tok * a.top_k + p0);
     }
-    float acc[2][kPass][2];
+    return;
+  }
+  if (rg * 16 >= a.f) return;
+  pdl_wait();
+  pdl_trigger();
+  const int4 wk = a.work[blockIdx.y];  // expert, first position, count (0 past the active ones)
+  const int e = wk.x, pos0 = wk.y, cnt = wk.z;
+  if (cnt == 0) return;
+  const uint8_t* w0 = a.gate + (size_t)e * a.mb_gu;
+  const uint8_t* w1 = a.up + (size_t)e * a.mb_gu;
+  const int n_kb = a.d / unit_k(FMT_R);
+  GuStage<FMT_R, P> s0, s1;
+  for (int p0 = 0; p0 < cnt; p0 += P) {
+    const int np = min(P, cnt - p0);
+    const __nv_bfloat16* xrow[P];
+    float sc[P];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) acc[m][tt][0] = acc[m][tt][1] = 0.f;
-    for (int kb = warp; kb < n_kb; kb += kWarps) {
-      if (fmt == FMT_Q2_K) {
-        const Q2kUnitRegs u0 = q2k_load(w0 + unit_offset(rg, kb, n_kb, kQ2kUnitBytes));
-        const Q2kUnitRegs u1 = q2k_load(w1 + unit_offset(rg, kb, n_kb, kQ2kUnitBytes));
-        float as[2][kPass][2], am[2][kPass][2];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) as[m][tt][0] = as[m][tt][1] = am[m][tt][0] = am[m][tt][1] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int kc = kb * 256 + 128 * c;
-          XFrag xf[kPass];
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt)
-            if (tt < np) xf[tt] = xfrag_bf16(xrow[tt] + kc, sc[tt]);
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const Q2kUnitRegs& u = m ? u1 : u0;
-            const uint32_t w[4] = {u.q[c].x, u.q[c].y, u.q[c].z, u.q[c].w};
-            const uint32_t wh[4] = {w[0] >> 10, w[1] >> 10, w[2] >> 10, w[3] >> 10};
-            const Q2kChunkScales s = q2k_chunk_scales(u.sc[c], qc);
-#pragma unroll
-            for (int tt = 0; tt < kPass; ++tt) {
-              if (tt >= np) break;
-              float dd[4];
-              q2k_chunk_mma(w, wh, bm, xf[tt], dd);
-              as[m][tt][0] = fmaf(s.s00, dd[0], fmaf(s.s01, dd[1], as[m][tt][0]));
-              as[m][tt][1] = fmaf(s.s10, dd[2], fmaf(s.s11, dd[3], as[m][tt][1]));
-              am[m][tt][0] = fmaf(s.m00, xf[tt].s0, fmaf(s.m01, xf[tt].s1, am[m][tt][0]));
-              am[m][tt][1] = fmaf(s.m10, xf[tt].s0, fmaf(s.m11, xf[tt].s1, am[m][tt][1]));
-            }
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const Q2kUnitRegs& u = m ? u1 : u0;
-          const float2 d0 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd0));
-          const float2 d1 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd1));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            acc[m][tt][0] = fmaf(d0.x, as[m][tt][0], fmaf(-d0.y, am[m][tt][0], acc[m][tt][0]));
-            acc[m][tt][1] = fmaf(d1.x, as[m][tt][1], fmaf(-d1.y, am[m][tt][1], acc[m][tt][1]));
-          }
-        }
-      } else {
-        const Q80UnitRegs u0 = q80_load(w0 + unit_offset(rg, kb, n_kb, kQ80UnitBytes));
-        const Q80UnitRegs u1 = q80_load(w1 + unit_offset(rg, kb, n_kb, kQ80UnitBytes));
-        const int kc = kb * 128;
-        XFrag xf[kPass];
-#pragma unroll
-        for (int tt = 0; tt < kPass; ++tt)
-          if (tt < np) xf[tt] = xfrag_bf16(xrow[tt] + kc, sc[tt]);
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const Q80UnitRegs& u = m ? u1 : u0;
-          const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&u.sc));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            float dd[4];
-            q80_chunk_mma(u.v, bm, xf[tt], dd);
-            const float off = 128.f * (xf[tt].s0 + xf[tt].s1);
-            acc[m][tt][0] = fmaf(s.x, fmaf(16777216.f, dd[0] + dd[1], -off), acc[m][tt][0]);
-            acc[m][tt][1] = fmaf(s.y, fmaf(16777216.f, dd[2] + dd[3], -off), acc[m][tt][1]);
-          }
-        }
-      }
+    for (int tt = 0; tt < P; ++tt) {
+      const int tok = a.tokof[pos0 + p0 + min(tt, np - 1)];
+      xrow[tt] = a.x + (size_t)tok * a.d;
+      sc[tt] = a.xscale[tok];
     }
-    // reduce the quad, then the warps in a fixed order
+    float accg[P][2], accu[P][2];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt)
-#pragma unroll
-        for (int rho = 0; rho < 2; ++rho) {
-          float v = acc[m][tt][rho];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (t == 0) red[warp][m][tt][g + 8 * rho] = v;
-        }
-    __syncthreads();
-    // whole warps take part (the 16-lane shuffles below name all 32 lanes): warp 0 for one
-    // token per pass, warps 0 and 1 for four
-    if (threadIdx.x < (kPass == 1 ? 32 : 16 * kPass)) {
-      const int tt = min(threadIdx.x >> 4, kPass - 1), r = threadIdx.x & 15;
-      const bool valid = (int)(threadIdx.x >> 4) < np;
-      float s0 = 0.f, s1 = 0.f;
-      for (int w = 0; w < kWarps; ++w) {
-        s0 += red[w][0][tt][r];
-        s1 += red[w][1][tt][r];
-      }
-      const float inv = 1.f / sc[tt];
-      const float h = valid ? silu_mul(s0 * inv, s1 * inv) : 0.f;
-      const int pos = pos0 + p0 + tt;
-      if (valid) {
-        float* hrow = shared ? a.Hs + (size_t)pos * a.fs : a.H + (size_t)pos * a.f;
-        hrow[rg * 16 + r] = h;
-      }
-      float m = fabsf(h);  // max over the 16 rows of this CTA (16 consecutive lanes)
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, 16));
-      if (valid && r == 0) {
-        unsigned* hm = reinterpret_cast<unsigned*>(a.hmax + (shared ? a.n_tok * a.top_k + pos : pos));
-        atomicMax(hm, __float_as_uint(m));  // non-negative floats order like their bit patterns
-      }
-    }
-    __syncthreads();
+    for (int tt = 0; tt < P; ++tt) accg[tt][0] = accg[tt][1] = accu[tt][0] = accu[tt][1] = 0.f;
+    gu_stream<FMT_R, P>(s0, s1, false, w0, w1, rg, n_kb, xrow, sc, np, bm, qc, accg, accu);
+    gu_epilogue<P>(red, accg, accu, sc, np, a.H, a.f, pos0 + p0, rg, a.hmax + pos0 + p0);
   }
 }
 
 // ----------------------------------------------------------------------------- down + combine
 
-template <int FMT_R, int FMT_S, int kPass>
-__global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int max_active) {
-  __shared__ float ys[kMaxTok * 16][16];     // per bucketed slot position
-  __shared__ float ysh[kWarps][kMaxTok][16];  // shared expert partials per warp
-  const int rg = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int nt = a.n_tok, K = a.top_k;
-  const int n_kb_r = a.f / unit_k(FMT_R), ub_r = unit_bytes(FMT_R);
-  const int n_kb_s = a.n_shared ? a.fs / unit_k(FMT_S) : 0, ub_s = unit_bytes(FMT_S);
-  // routing is final (its kernel completed before the gate/up kernel passed its wait): stream
-  // this CTA's rows of every touched expert, and of the shared expert, into L2 now
-  {
-    const int n_act = *a.n_active;
-    for (int item = warp; item < n_act * n_kb_r; item += kWarps) {
-      const int e = a.active[item / n_kb_r], kb = item % n_kb_r;
-      prefetch_l2(a.down + (size_t)e * a.mb_d + unit_offset(rg, kb, n_kb_r, ub_r), ub_r);
-    }
-    for (int kb = warp; kb < n_kb_s; kb += kWarps) prefetch_l2(a.sdown + unit_offset(rg, kb, n_kb_s, ub_s), ub_s);
+// Item i of a CTA: routed items first (work entry i / n_kb_r, K unit i % n_kb_r), then the
+// shared expert's K units.
+struct DownItem {
+  int shared, kb, pos0, cnt;
+  const uint8_t* w;
+};
+
+__device__ __forceinline__ DownItem down_item(const DecodeArgs& a, int i, int n_routed, int n_kb_r) {
+  DownItem it;
+  it.shared = i >= n_routed;
+  if (!it.shared) {
+    const int4 wk = a.work[i / n_kb_r];
+    it.kb = i % n_kb_r;
+    it.pos0 = wk.y;
+    it.cnt = wk.z;
+    it.w = a.down + (size_t)wk.x * a.mb_d;
+  } else {
+    it.kb = i - n_routed;
+    it.pos0 = 0;
+    it.cnt = a.n_tok;
+    it.w = a.sdown;
   }
-  pdl_wait();
-  const int n_act = *a.n_active;
+  return it;
+}
+
+// One item: the unit times the item's h rows (in passes of 4), added to the warp's partial rows.
+template <int FMT, int P>
+__device__ __forceinline__ void down_item_compute(const DecodeArgs& a, const DownItem& it, const Unit<FMT>& u,
+                                                  float* part_rows, const BMask& bm, const Q2kLaneConst& qc,
+                                                  int kdim) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* hbase = it.shared ? a.Hs : a.H;
+  const float* hmax = it.shared ? a.hmax + a.n_tok * a.top_k : a.hmax;
+  for (int p0 = 0; p0 < it.cnt; p0 += P) {
+    const int np = min(P, it.cnt - p0);
+    float sc[P];
+    XFrag xf[P][2];
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) {
+      if (tt >= np) break;
+      const int row = it.pos0 + p0 + tt;
+      sc[tt] = fp16_row_scale(__ldcg(hmax + row));
+#pragma unroll
+      for (int c = 0; c < Unit<FMT>::kChunks; ++c)
+        xf[tt][c] = xfrag_f32(hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c, sc[tt]);
+    }
+    float acc[P][2];
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) acc[tt][0] = acc[tt][1] = 0.f;
+    unit_mma<P>(u, xf, np, bm, qc, acc);
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) {
+      if (tt >= np) break;
+#pragma unroll
+      for (int rho = 0; rho < 2; ++rho) {
+        float v = acc[tt][rho];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (t == 0) part_rows[(size_t)(it.pos0 + p0 + tt) * 16 + g + 8 * rho] += v / sc[tt];
+      }
+    }
+  }
+}
+
+// Registers of one loaded unit of either format (a Q8_0 unit fills v[0..3] and w[0]; a Q2_K
+// unit fills v[0..1] and w[0..3]), so that both item kinds share one pipeline buffer.
+struct RawUnit {
+  uint4 v[4];
+  uint32_t w[4];
+};
+
+template <int FMT>
+__device__ __forceinline__ void raw_load(RawUnit& b, const uint8_t* __restrict__ ub) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  if (FMT == FMT_Q2_K) {
+    b.v[0] = ldg_nc_v4(ub + 16 * lane);
+    b.v[1] = ldg_nc_v4(ub + 512 + 16 * lane);
+    b.w[0] = ldg_nc_u32(ub + kQ2kScOff + 4 * lane);
+    b.w[1] = ldg_nc_u32(ub + kQ2kScOff + 128 + 4 * lane);
+    b.w[2] = ldg_nc_u32(ub + kQ2kDdOff + 4 * g);
+    b.w[3] = ldg_nc_u32(ub + kQ2kDdOff + 4 * (g + 8));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) b.v[j] = ldg_nc_v4(ub + 512 * j + 16 * lane);
+    b.w[0] = ldg_nc_u32(ub + kQ80ScOff + 4 * lane);
+  }
+}
+
+__device__ __forceinline__ Unit<FMT_Q2_K> as_q2k(const RawUnit& b) {
+  Unit<FMT_Q2_K> u;
+  u.r.q[0] = b.v[0];
+  u.r.q[1] = b.v[1];
+  u.r.sc[0] = b.w[0];
+  u.r.sc[1] = b.w[1];
+  u.r.dd0 = b.w[2];
+  u.r.dd1 = b.w[3];
+  return u;
+}
+
+__device__ __forceinline__ Unit<FMT_Q8_0> as_q80(const RawUnit& b) {
+  Unit<FMT_Q8_0> u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u.r.v[j] = b.v[j];
+  u.r.sc = b.w[0];
+  return u;
+}
+
+template <int FMT>
+__device__ __forceinline__ Unit<FMT> as_unit(const RawUnit& b);
+template <>
+__device__ __forceinline__ Unit<FMT_Q2_K> as_unit<FMT_Q2_K>(const RawUnit& b) { return as_q2k(b); }
+template <>
+__device__ __forceinline__ Unit<FMT_Q8_0> as_unit<FMT_Q8_0>(const RawUnit& b) { return as_q80(b); }
+
+template <int FMT_R, int FMT_S>
+__device__ __forceinline__ void down_load(const DownItem& it, RawUnit& b, int rg, int n_kb_r, int n_kb_s) {
+  if (it.shared)
+    raw_load<FMT_S>(b, it.w + unit_offset(rg, it.kb, n_kb_s, unit_bytes(FMT_S)));
+  else
+    raw_load<FMT_R>(b, it.w + unit_offset(rg, it.kb, n_kb_r, unit_bytes(FMT_R)));
+}
+
+template <int FMT_R, int FMT_S, int P>
+__device__ __forceinline__ void down_item_run(const DecodeArgs& a, const DownItem& it, const RawUnit& b, float* part,
+                                              float* parts, const BMask& bm, const Q2kLaneConst& qc) {
+  if (it.shared)
+    down_item_compute<FMT_S, P>(a, it, as_unit<FMT_S>(b), parts, bm, qc, a.fs);
+  else
+    down_item_compute<FMT_R, P>(a, it, as_unit<FMT_R>(b), part, bm, qc, a.f);
+}
+
+template <int FMT_R, int FMT_S, int P>
+__global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int max_active) {
+  extern __shared__ __align__(16) float dsm[];
+  const int rg = blockIdx.x, warp = threadIdx.x >> 5;
+  const int nt = a.n_tok, K = a.top_k, n_slots = nt * K;
+  float* part = dsm + (size_t)warp * n_slots * 16;                               // [warp][position][16]
+  float* parts = dsm + (size_t)kWarps * n_slots * 16 + (size_t)warp * nt * 16;  // [warp][token][16]
+  const int n_kb_r = a.f / unit_k(FMT_R);
+  const int n_kb_s = a.n_shared ? a.fs / unit_k(FMT_S) : 0;
   const BMask bm;
   const Q2kLaneConst qc;
-  // routed: warp w takes the touched experts w, w+8, ... over the full K
-  for (int ai = warp; ai < n_act; ai += kWarps) {
-    const int e = a.active[ai];
-    const int pos0 = a.offsets[e], cnt = a.offsets[e + 1] - pos0;
-    const uint8_t* wd = a.down + (size_t)e * a.mb_d;
-    for (int p0 = 0; p0 < cnt; p0 += kPass) {
-      const int np = min(kPass, cnt - p0);
-      const float* hrow[kPass];
-      float sc[kPass];
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) {
-        const int pos = pos0 + p0 + min(tt, np - 1);
-        hrow[tt] = a.H + (size_t)pos * a.f;
-        sc[tt] = fp16_row_scale(__ldcg(a.hmax + pos));
-      }
-      float acc[kPass][2];
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) acc[tt][0] = acc[tt][1] = 0.f;
-      for (int kb = 0; kb < n_kb_r; ++kb) {
-        if (FMT_R == FMT_Q2_K) {
-          const Q2kUnitRegs u = q2k_load(wd + unit_offset(rg, kb, n_kb_r, kQ2kUnitBytes));
-          float as[kPass][2], am[kPass][2];
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) as[tt][0] = as[tt][1] = am[tt][0] = am[tt][1] = 0.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int kc = kb * 256 + 128 * c;
-            const uint32_t w[4] = {u.q[c].x, u.q[c].y, u.q[c].z, u.q[c].w};
-            const uint32_t wh[4] = {w[0] >> 10, w[1] >> 10, w[2] >> 10, w[3] >> 10};
-            const Q2kChunkScales s = q2k_chunk_scales(u.sc[c], qc);
-#pragma unroll
-            for (int tt = 0; tt < kPass; ++tt) {
-              if (tt >= np) break;
-              const XFrag xf = xfrag_f32(hrow[tt] + kc, sc[tt]);
-              float dd[4];
-              q2k_chunk_mma(w, wh, bm, xf, dd);
-              as[tt][0] = fmaf(s.s00, dd[0], fmaf(s.s01, dd[1], as[tt][0]));
-              as[tt][1] = fmaf(s.s10, dd[2], fmaf(s.s11, dd[3], as[tt][1]));
-              am[tt][0] = fmaf(s.m00, xf.s0, fmaf(s.m01, xf.s1, am[tt][0]));
-              am[tt][1] = fmaf(s.m10, xf.s0, fmaf(s.m11, xf.s1, am[tt][1]));
-            }
-          }
-          const float2 d0 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd0));
-          const float2 d1 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd1));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            acc[tt][0] = fmaf(d0.x, as[tt][0], fmaf(-d0.y, am[tt][0], acc[tt][0]));
-            acc[tt][1] = fmaf(d1.x, as[tt][1], fmaf(-d1.y, am[tt][1], acc[tt][1]));
-          }
-        } else {
-          const Q80UnitRegs u = q80_load(wd + unit_offset(rg, kb, n_kb_r, kQ80UnitBytes));
-          const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&u.sc));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            const XFrag xf = xfrag_f32(hrow[tt] + kb * 128, sc[tt]);
-            float dd[4];
-            q80_chunk_mma(u.v, bm, xf, dd);
-            const float off = 128.f * (xf.s0 + xf.s1);
-            acc[tt][0] = fmaf(s.x, fmaf(16777216.f, dd[0] + dd[1], -off), acc[tt][0]);
-            acc[tt][1] = fmaf(s.y, fmaf(16777216.f, dd[2] + dd[3], -off), acc[tt][1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) {
-        if (tt >= np) break;
-#pragma unroll
-        for (int rho = 0; rho < 2; ++rho) {
-          float v = acc[tt][rho];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (t == 0) ys[pos0 + p0 + tt][g + 8 * rho] = v / sc[tt];
-        }
-      }
-    }
+  for (int i = threadIdx.x & 31; i < n_slots * 16; i += 32) part[i] = 0.f;
+  for (int i = threadIdx.x & 31; i < nt * 16; i += 32) parts[i] = 0.f;
+  // The routing is final once this kernel runs (its kernel completed before the gate/up kernel
+  // passed its wait): the work list is valid, and the first down units can be loaded right away.
+  const int n_act = *a.n_active;
+  const int n_routed = n_act * n_kb_r, n_items = n_routed + n_kb_s;
+  RawUnit b0, b1;
+  DownItem it0{}, it1{};
+  if (warp < n_items) {
+    it0 = down_item(a, warp, n_routed, n_kb_r);
+    down_load<FMT_R, FMT_S>(it0, b0, rg, n_kb_r, n_kb_s);
   }
-  // shared expert: every warp takes a slice of K for all tokens
-  if (a.n_shared) {
-    for (int p0 = 0; p0 < nt; p0 += kPass) {
-      const int np = min(kPass, nt - p0);
-      const float* hrow[kPass];
-      float sc[kPass];
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) {
-        const int tok = p0 + min(tt, np - 1);
-        hrow[tt] = a.Hs + (size_t)tok * a.fs;
-        sc[tt] = fp16_row_scale(__ldcg(a.hmax + nt * K + tok));
-      }
-      float acc[kPass][2];
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) acc[tt][0] = acc[tt][1] = 0.f;
-      for (int kb = warp; kb < n_kb_s; kb += kWarps) {
-        if (FMT_S == FMT_Q2_K) {
-          const Q2kUnitRegs u = q2k_load(a.sdown + unit_offset(rg, kb, n_kb_s, kQ2kUnitBytes));
-          float as[kPass][2], am[kPass][2];
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) as[tt][0] = as[tt][1] = am[tt][0] = am[tt][1] = 0.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int kc = kb * 256 + 128 * c;
-            const uint32_t w[4] = {u.q[c].x, u.q[c].y, u.q[c].z, u.q[c].w};
-            const uint32_t wh[4] = {w[0] >> 10, w[1] >> 10, w[2] >> 10, w[3] >> 10};
-            const Q2kChunkScales s = q2k_chunk_scales(u.sc[c], qc);
-#pragma unroll
-            for (int tt = 0; tt < kPass; ++tt) {
-              if (tt >= np) break;
-              const XFrag xf = xfrag_f32(hrow[tt] + kc, sc[tt]);
-              float dd[4];
-              q2k_chunk_mma(w, wh, bm, xf, dd);
-              as[tt][0] = fmaf(s.s00, dd[0], fmaf(s.s01, dd[1], as[tt][0]));
-              as[tt][1] = fmaf(s.s10, dd[2], fmaf(s.s11, dd[3], as[tt][1]));
-              am[tt][0] = fmaf(s.m00, xf.s0, fmaf(s.m01, xf.s1, am[tt][0]));
-              am[tt][1] = fmaf(s.m10, xf.s0, fmaf(s.m11, xf.s1, am[tt][1]));
-            }
-          }
-          const float2 d0 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd0));
-          const float2 d1 = __half22float2(*reinterpret_cast<const __half2*>(&u.dd1));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            acc[tt][0] = fmaf(d0.x, as[tt][0], fmaf(-d0.y, am[tt][0], acc[tt][0]));
-            acc[tt][1] = fmaf(d1.x, as[tt][1], fmaf(-d1.y, am[tt][1], acc[tt][1]));
-          }
-        } else {
-          const Q80UnitRegs u = q80_load(a.sdown + unit_offset(rg, kb, n_kb_s, kQ80UnitBytes));
-          const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&u.sc));
-#pragma unroll
-          for (int tt = 0; tt < kPass; ++tt) {
-            if (tt >= np) break;
-            const XFrag xf = xfrag_f32(hrow[tt] + kb * 128, sc[tt]);
-            float dd[4];
-            q80_chunk_mma(u.v, bm, xf, dd);
-            const float off = 128.f * (xf.s0 + xf.s1);
-            acc[tt][0] = fmaf(s.x, fmaf(16777216.f, dd[0] + dd[1], -off), acc[tt][0]);
-            acc[tt][1] = fmaf(s.y, fmaf(16777216.f, dd[2] + dd[3], -off), acc[tt][1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int tt = 0; tt < kPass; ++tt) {
-        if (tt >= np) break;
-#pragma unroll
-        for (int rho = 0; rho < 2; ++rho) {
-          float v = acc[tt][rho];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (t == 0) ysh[warp][p0 + tt][g + 8 * rho] = v / sc[tt];
-        }
+  if (warp + kWarps < n_items) {
+    it1 = down_item(a, warp + kWarps, n_routed, n_kb_r);
+    down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
+  }
+  pdl_wait();
+  for (int i = warp; i < n_items; i += 2 * kWarps) {
+    down_item_run<FMT_R, FMT_S, P>(a, it0, b0, part, parts, bm, qc);
+    if (i + 2 * kWarps < n_items) {
+      it0 = down_item(a, i + 2 * kWarps, n_routed, n_kb_r);
+      down_load<FMT_R, FMT_S>(it0, b0, rg, n_kb_r, n_kb_s);
+    }
+    if (i + kWarps < n_items) {
+      down_item_run<FMT_R, FMT_S, P>(a, it1, b1, part, parts, bm, qc);
+      if (i + 3 * kWarps < n_items) {
+        it1 = down_item(a, i + 3 * kWarps, n_routed, n_kb_r);
+        down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
       }
     }
   }
   __syncthreads();
-  // combine: out[t][r] = sum over the token's slots in ascending expert id, then the shared expert
+  // combine: out[t][r] = routed terms in ascending expert id (each the fixed-order sum of the
+  // warps' partials), then the shared expert
+  const float* part0 = dsm;
+  const float* parts0 = dsm + (size_t)kWarps * n_slots * 16;
   if (threadIdx.x < nt * 16) {
     const int tok = threadIdx.x >> 4, r = threadIdx.x & 15;
     int ex[16], ps[16];
@@ -537,11 +627,14 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int
       ex[i] = ej; wv[i] = wj; ps[i] = pj;
     }
     float o = 0.f;
-    for (int j = 0; j < K; ++j) o = fmaf(wv[j], ys[ps[j]][r], o);
+    for (int j = 0; j < K; ++j) {
+      float y = 0.f;
+      for (int w = 0; w < kWarps; ++w) y += part0[((size_t)w * n_slots + ps[j]) * 16 + r];
+      o = fmaf(wv[j], y, o);
+    }
     if (a.n_shared) {
       float s = 0.f;
-      for (int w = 0; w < kWarps; ++w)
-        if (w < n_kb_s) s += ysh[w][tok][r];
+      for (int w = 0; w < kWarps; ++w) s += parts0[((size_t)w * nt + tok) * 16 + r];
       o += s;
     }
     a.out[(size_t)tok * a.d + rg * 16 + r] = o;
@@ -549,11 +642,12 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int
 }
 
 template <typename Kern>
-cudaError_t launch_pdl(Kern kernel, dim3 grid, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
+cudaError_t launch_ex(Kern kernel, dim3 grid, size_t smem, cudaStream_t s, bool pdl, const DecodeArgs& a,
+                      int max_active) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -563,40 +657,55 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, cudaStream_t s, bool pdl, const D
   return cudaLaunchKernelEx(&cfg, kernel, a, max_active);
 }
 
+template <int R, int S>
+cudaError_t launch_gu(dim3 grid, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
+  return a.n_tok == 1 ? launch_ex(gateup_decode_kernel<R, S, 1>, grid, 0, s, pdl, a, max_active)
+                      : launch_ex(gateup_decode_kernel<R, S, 2>, grid, 0, s, pdl, a, max_active);
+}
+
+template <int R, int S, int P>
+cudaError_t launch_dn_p(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(down_decode_kernel<R, S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    attr_set = true;
+  }
+  return launch_ex(down_decode_kernel<R, S, P>, grid, smem, s, pdl, a, max_active);
+}
+
+template <int R, int S>
+cudaError_t launch_dn(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
+  return a.n_tok == 1 ? launch_dn_p<R, S, 1>(grid, smem, s, pdl, a, max_active)
+                      : launch_dn_p<R, S, 2>(grid, smem, s, pdl, a, max_active);
+}
+
 }  // namespace
 
 int decode_max_tokens() { return kMaxTok; }
+int decode_max_slots() { return kMaxSlots; }
 
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks) {
   const int max_active = min(a.n_exp, a.n_tok * a.top_k);
   route_decode_kernel<<<a.n_exp, kThreads, 0, s>>>(a);
-  if (hooks) hooks->mark(hooks->ctx, "route");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 g_gu((max(a.f, a.n_shared ? a.fs : 0)) / 16, max_active + (a.n_shared ? 1 : 0));
+  if (hooks) hooks->mark(hooks->ctx, "route");
+  const dim3 g_gu(max(a.f, a.n_shared ? a.fs : 0) / 16, max_active + (a.n_shared ? 1 : 0));
   const int fsg = a.n_shared ? fmt_s : fmt_r_gu;
-  const bool one = a.n_tok == 1;
-#define DS4_GU(R, S)                                                                          \
-  e = one ? launch_pdl(gateup_decode_kernel<R, S, 1>, g_gu, s, pdl, a, max_active)            \
-          : launch_pdl(gateup_decode_kernel<R, S, 4>, g_gu, s, pdl, a, max_active)
-  if (fmt_r_gu == FMT_Q2_K && fsg == FMT_Q2_K) DS4_GU(FMT_Q2_K, FMT_Q2_K);
-  else if (fmt_r_gu == FMT_Q2_K) DS4_GU(FMT_Q2_K, FMT_Q8_0);
-  else if (fsg == FMT_Q2_K) DS4_GU(FMT_Q8_0, FMT_Q2_K);
-  else DS4_GU(FMT_Q8_0, FMT_Q8_0);
-#undef DS4_GU
+  if (fmt_r_gu == FMT_Q2_K && fsg == FMT_Q2_K) e = launch_gu<FMT_Q2_K, FMT_Q2_K>(g_gu, s, pdl, a, max_active);
+  else if (fmt_r_gu == FMT_Q2_K) e = launch_gu<FMT_Q2_K, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
+  else if (fsg == FMT_Q2_K) e = launch_gu<FMT_Q8_0, FMT_Q2_K>(g_gu, s, pdl, a, max_active);
+  else e = launch_gu<FMT_Q8_0, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "gateup");
   const int fsd = a.n_shared ? fmt_s : fmt_r_d;
   const dim3 g_dn(a.d / 16);
-#define DS4_DN(R, S)                                                                          \
-  e = one ? launch_pdl(down_decode_kernel<R, S, 1>, g_dn, s, pdl, a, max_active)              \
-          : launch_pdl(down_decode_kernel<R, S, 4>, g_dn, s, pdl, a, max_active)
-  if (fmt_r_d == FMT_Q2_K && fsd == FMT_Q2_K) DS4_DN(FMT_Q2_K, FMT_Q2_K);
-  else if (fmt_r_d == FMT_Q2_K) DS4_DN(FMT_Q2_K, FMT_Q8_0);
-  else if (fsd == FMT_Q2_K) DS4_DN(FMT_Q8_0, FMT_Q2_K);
-  else DS4_DN(FMT_Q8_0, FMT_Q8_0);
-#undef DS4_DN
+  const size_t smem = (size_t)kWarps * (a.n_tok * a.top_k + a.n_tok) * 16 * sizeof(float);
+  if (fmt_r_d == FMT_Q2_K && fsd == FMT_Q2_K) e = launch_dn<FMT_Q2_K, FMT_Q2_K>(g_dn, smem, s, pdl, a, max_active);
+  else if (fmt_r_d == FMT_Q2_K) e = launch_dn<FMT_Q2_K, FMT_Q8_0>(g_dn, smem, s, pdl, a, max_active);
+  else if (fsd == FMT_Q2_K) e = launch_dn<FMT_Q8_0, FMT_Q2_K>(g_dn, smem, s, pdl, a, max_active);
+  else e = launch_dn<FMT_Q8_0, FMT_Q8_0>(g_dn, smem, s, pdl, a, max_active);
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "down_combine");
   if (launches) *launches = 3;

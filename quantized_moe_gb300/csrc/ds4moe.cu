@@ -96,6 +96,9 @@ struct ds4moe_handle {
   int* err = nullptr;
   float* xmax = nullptr;
   float* hmax = nullptr;
+  int4* work = nullptr;
+  int* tokof = nullptr;
+  float* xscale = nullptr;
   unsigned int* counter = nullptr;
   // host-call staging
   __nv_bfloat16* x_stage = nullptr;
@@ -318,6 +321,9 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->xmax, M * 4));
   DS4_TRY(h->alloc_t(&h->hmax, (slots + M) * 4));
   DS4_TRY(h->alloc_t(&h->counter, 4));
+  DS4_TRY(h->alloc_t(&h->work, (size_t)E * sizeof(int4)));
+  DS4_TRY(h->alloc_t(&h->tokof, slots * 4));
+  DS4_TRY(h->alloc_t(&h->xscale, M * 4));
   DS4_TRY(h->alloc_t(&h->x_stage, M * d * 2));
   DS4_TRY(h->alloc_t(&h->tid_stage, M * 4));
   DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
@@ -371,7 +377,7 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
       cudaEventRecord(h->ev[++phase], st);
     }
   };
-  if (n <= ds4::decode_max_tokens()) {
+  if (n <= ds4::decode_max_tokens() && n * K <= ds4::decode_max_slots()) {
     // decode path: three kernels, chained with programmatic dependent launch unless profiling
     ds4::DecodeArgs da{};
     da.x = xb; da.n_tok = n; da.d = d; da.wr = h->router_w; da.br = h->router_b; da.n_exp = E; da.top_k = K;
@@ -379,6 +385,7 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
     da.logits = h->logits; da.xmax = h->xmax; da.idx = h->idx; da.wts = h->wts; da.counts = h->counts;
     da.offsets = h->offsets; da.active = h->active; da.n_active = h->n_active; da.perm = h->perm;
     da.rowof = h->rowof; da.err = h->err; da.counter = h->counter; da.hmax = h->hmax;
+    da.work = h->work; da.tokof = h->tokof; da.xscale = h->xscale;
     da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = f;
     da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
     da.fs = fs; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
@@ -488,7 +495,8 @@ extern "C" int64_t ds4moe_device_bytes(const ds4moe_handle* h) { return h ? h->b
 
 extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n_tokens) {
   if (!h || n_tokens <= 0) return 0;
-  if (n_tokens <= ds4::decode_max_tokens()) return 3;  // route, gate/up, down + combine
+  if (n_tokens <= ds4::decode_max_tokens() && n_tokens * h->s.top_k <= ds4::decode_max_slots())
+    return 3;  // route, gate/up, down + combine
   // router, top-k, 2 bucketing, gate/up + down routed, the same for shared, combine
   return 1 + 1 + 2 + 2 + (h->s.n_shared ? 2 : 0) + 1;
 }

@@ -28,6 +28,32 @@ __device__ __forceinline__ void xfrag_sums(XFrag& f, float p) {
   f.s1 = __shfl_sync(0xffffffffu, p, 8 * t + 4);
 }
 
+// Raw (unconverted) activation words of one lane for one chunk: bf16 pairs at k = 16g + 2t
+// and 16g + 2t + 8. Loading them early and converting later keeps the load off the critical path.
+__device__ __forceinline__ uint2 xraw_bf16(const __nv_bfloat16* __restrict__ chunk) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  return make_uint2(*reinterpret_cast<const uint32_t*>(chunk + 16 * g + 2 * t),
+                    *reinterpret_cast<const uint32_t*>(chunk + 16 * g + 2 * t + 8));
+}
+
+__device__ __forceinline__ XFrag xfrag_from_bf16(uint2 raw, float sc) {
+  const float2 v0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+  const float2 v1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+  const __half2 h0 = __floats2half2_rn(v0.x * sc, v0.y * sc);
+  const __half2 h1 = __floats2half2_rn(v1.x * sc, v1.y * sc);
+  XFrag f;
+  f.b0 = *reinterpret_cast<const uint32_t*>(&h0);
+  f.b1 = *reinterpret_cast<const uint32_t*>(&h1);
+  const float2 a = __half22float2(h0), b = __half22float2(h1);
+  float p = (a.x + a.y) + (b.x + b.y);
+  const int t = threadIdx.x & 3;
+  p += __shfl_xor_sync(0xffffffffu, p, 1);
+  p += __shfl_xor_sync(0xffffffffu, p, 2);
+  f.s0 = __shfl_sync(0xffffffffu, p, 8 * t);
+  f.s1 = __shfl_sync(0xffffffffu, p, 8 * t + 4);
+  return f;
+}
+
 // From a bf16 row (chunk base pointer), scaled by sc.
 __device__ __forceinline__ XFrag xfrag_bf16(const __nv_bfloat16* __restrict__ chunk, float sc) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
