@@ -84,14 +84,18 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
       a.xmax[t] = m;
     }
   }
-  // ---- arrival: the last CTA continues with the top-k and the bucketing
-  __threadfence();
+  // ---- arrival: the last CTA continues with the top-k and the bucketing. The barrier orders the
+  // CTA's writes before thread 0's release-acquire arrival, whose gpu-scope ordering covers them.
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.counter) : "memory");
+    s_last = prev == gridDim.x - 1;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int K = a.top_k, E = a.n_exp, n_slots = nt * K;
+  if (threadIdx.x == 0) *a.err = 0;  // only this CTA writes the error word
   for (int t = warp; t < nt; t += kWarps) {
     if (t < a.n_hash) {
       const int id = a.token_ids[t];

@@ -104,6 +104,10 @@ struct ds4moe_handle {
   __nv_bfloat16* x_stage = nullptr;
   int* tid_stage = nullptr;
   float* out_stage = nullptr;
+  // device pointers already verified by a forward (a small ring)
+  static constexpr int kChecked = 32;
+  const void* checked[kChecked] = {};
+  int checked_next = 0;
   // last forward
   cudaStream_t last_stream = nullptr;
   int last_n = 0;
@@ -358,9 +362,14 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   const char* names[3] = {"x", "out", "token_ids"};
   for (int i = 0; i < 3; ++i) {
     if (!ptrs[i]) continue;
+    bool seen = false;  // pointers already verified on this handle skip the driver query
+    for (const void* p : h->checked)
+      if (p == ptrs[i]) seen = true;
+    if (seen) continue;
     const PtrKind k = classify(ptrs[i], s.device);
     if (k == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than the handle's (%d)", names[i], s.device);
     if (k != PTR_DEVICE) return fail(DS4MOE_ERR_INVALID_ARG, "%s is not device memory (use ds4moe_forward_host for host buffers)", names[i]);
+    h->checked[h->checked_next++ % ds4moe_handle::kChecked] = ptrs[i];
   }
   DeviceGuard guard(s.device);
   if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", s.device);
@@ -368,7 +377,6 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   const int E = s.n_experts, K = s.top_k, d = s.d, f = s.f_routed, fs = s.f_shared;
   const int n_learned = n - n_hash;
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
   int phase = 0;
   if (h->profile) DS4_CUDA(cudaEventRecord(h->ev[0], st));
   auto mark = [&](const char* name) {
@@ -405,6 +413,7 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
     ds4::launch_router_logits(xb + (size_t)n_hash * d, n_learned, d, h->router_w, h->router_b, E, h->logits, st);
     mark("router_logits");
   }
+  DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
   ds4::launch_topk(h->logits, n_learned, E, K, token_ids, n_hash, h->table, s.hash_vocab, h->idx, h->wts, h->err, st);
   mark("topk");
   ds4::launch_bucket_count(h->idx, n * K, E, h->counts, st);
