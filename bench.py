@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=8, help="distinct input batches cycled over the steps")
+    ap.add_argument("--l2-mode", choices=["layer", "flush"], default="layer",
+                    help="between steps: flush L2 then run a second layer (default), or flush only")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -255,6 +257,16 @@ def main():
               problem.shared_gate, problem.shared_up, problem.shared_down, problem.hash_table]
     h = api.ds4moe_create(api.make_weights(*arrays), shapes)
     del arrays
+    # A second layer of the same shape with its own weights: between timed steps it runs once
+    # after the L2 flush, as the previous layer of a model would, so the kernels' code is warm
+    # while every byte of the timed layer's data is cold.
+    h_prev = None
+    if args.l2_mode == "layer":
+        pp = synthetic.make_problem(spec.with_(seed=spec.seed + 1000003))
+        arrays = [pp.router_w, pp.router_b, pp.gate.full(), pp.up.full(), pp.down.full(), pp.shared_gate,
+                  pp.shared_up, pp.shared_down, pp.hash_table]
+        h_prev = api.ds4moe_create(api.make_weights(*arrays), shapes)
+        del arrays, pp
 
     # per-rank input batches (different tokens per step, and per rank)
     xs, tids = [], []
@@ -268,35 +280,47 @@ def main():
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
 
-    def fwd(i):
+    out_prev = torch.empty_like(out)
+
+    def fwd(i, handle=None, o=None):
         b = i % args.batches
-        api.ds4moe_forward_ex(h, xs[b].data_ptr(), spec.n_tokens, tids[b].data_ptr() if spec.n_hash else None,
-                              spec.n_hash, out.data_ptr(), stream.cuda_stream)
+        api.ds4moe_forward_ex(handle or h, xs[b].data_ptr(), spec.n_tokens,
+                              tids[b].data_ptr() if spec.n_hash else None, spec.n_hash,
+                              (o if o is not None else out).data_ptr(), stream.cuda_stream)
+
+    def cool(i):
+        flush_buf.zero_()  # evicts everything from L2
+        if h_prev is not None:
+            fwd(i + 1, h_prev, out_prev)  # the previous layer: other weights, same kernels
+
+    def time_steps(n, prep):
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            prep(i)
+            st[i].record(stream)
+            fwd(i)
+            en[i].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(st, en)]
 
     for i in range(args.warmup):
-        flush_buf.zero_()
+        cool(i)
         fwd(i)
     torch.cuda.synchronize()
 
-    # timed region: each step timed alone with events on the launching stream, L2 flushed between
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # timed region: each step timed alone with events on the launching stream (L2 prepared
+    # before each step as above, outside the events)
     sampler = ClockSampler(local) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-    for i in range(args.steps):
-        flush_buf.zero_()
-        starts[i].record(stream)
-        fwd(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    step_ms = time_steps(args.steps, cool)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = float(sum(step_ms))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -308,11 +332,12 @@ def main():
 
     # per-launch times of the same workload: events recorded between the launches (this
     # serialises the launches, so it runs after the timed region, over the same inputs)
+    flush_only_ms = time_steps(args.steps, lambda i: flush_buf.zero_())  # code cold as well
     api.ds4moe_set_profiling(h, True)
     phase_ms: dict[str, list] = {}
     distinct = []
     for i in range(args.steps):
-        flush_buf.zero_()
+        cool(i)
         fwd(i)
         for name, ms in api.ds4moe_get_phase_times(h):  # waits for this step
             phase_ms.setdefault(name, []).append(ms)
@@ -326,7 +351,7 @@ def main():
     tid_host = tids[0].cpu().pin_memory() if spec.n_hash else None
     e2e_s = []
     for i in range(args.warmup + args.steps):
-        flush_buf.zero_()
+        cool(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         api.ds4moe_forward_host(h, x_host.data_ptr(), spec.n_tokens, tid_host.data_ptr() if tid_host is not None else None,
@@ -342,6 +367,8 @@ def main():
 
     launches = api.ds4moe_launches_per_forward(h, spec.n_tokens) * args.steps
     api.ds4moe_destroy(h)
+    if h_prev is not None:
+        api.ds4moe_destroy(h_prev)
 
     if rank != 0:
         if world > 1:
@@ -391,7 +418,10 @@ def main():
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 mma, f32 accumulate", "data": "synthetic",
-        "config": {"workload": workload_name(spec), "l2": "flushed between steps (write of 2x L2)",
+        "config": {"workload": workload_name(spec),
+                   "l2": ("flushed between steps (write of 2x L2), then one forward of a second layer with its own "
+                          "weights (kernel code warm, every byte of the timed layer cold)"
+                          if h_prev is not None else "flushed between steps (write of 2x L2)"),
                    "parallelism": f"replicas x{world}", "batches": args.batches},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -400,6 +430,7 @@ def main():
         "gpu_launches": launches,
         "clocks": clocks,
         "detail": {"step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+                   "ms_per_step_flush_only": float(np.mean(flush_only_ms)),
                    "phase_ms": mean_phase, "phase_share": share, "distinct_experts_mean": d_mean,
                    "forward_algorithmic_bytes": fwd_bytes, "forward_gbs": fwd_bytes / (ms_per_step / 1e3) / 1e9,
                    "forward_hbm_frac": fwd_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm"],
