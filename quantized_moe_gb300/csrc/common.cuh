@@ -188,6 +188,7 @@ struct DecodeHooks {
 };
 
 int decode_max_tokens();
+cudaError_t decode_prepare();  // sets kernel attributes once per device (not inside a capture)
 int decode_max_slots();
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks);

@@ -669,12 +669,15 @@ cudaError_t launch_gu(dim3 grid, cudaStream_t s, bool pdl, const DecodeArgs& a, 
 
 template <int R, int S, int P>
 cudaError_t launch_dn_p(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(down_decode_kernel<R, S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    attr_set = true;
-  }
   return launch_ex(down_decode_kernel<R, S, P>, grid, smem, s, pdl, a, max_active);
+}
+
+template <int R, int S>
+cudaError_t prepare_dn() {
+  cudaError_t e = cudaFuncSetAttribute(down_decode_kernel<R, S, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_decode_kernel<R, S, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  return e;
 }
 
 template <int R, int S>
@@ -684,6 +687,14 @@ cudaError_t launch_dn(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const De
 }
 
 }  // namespace
+
+cudaError_t decode_prepare() {
+  cudaError_t e = prepare_dn<FMT_Q2_K, FMT_Q2_K>();
+  if (e == cudaSuccess) e = prepare_dn<FMT_Q2_K, FMT_Q8_0>();
+  if (e == cudaSuccess) e = prepare_dn<FMT_Q8_0, FMT_Q2_K>();
+  if (e == cudaSuccess) e = prepare_dn<FMT_Q8_0, FMT_Q8_0>();
+  return e;
+}
 
 int decode_max_tokens() { return kMaxTok; }
 int decode_max_slots() { return kMaxSlots; }

@@ -118,6 +118,37 @@ struct ds4moe_handle {
   const char* phase_name[kMaxPhases] = {};
   int n_phases = 0;
 
+  // Decode forwards replay a captured CUDA graph of their three launches (launching each kernel
+  // from the host costs far more than a graph node). Graphs are keyed by the call's token
+  // counts and buffer pointers; at most kGraphs are kept, the least recently used is replaced.
+  bool use_graphs = true;
+  cudaStream_t cap_stream = nullptr;
+  struct GraphEntry {
+    int n = -1, n_hash = 0;
+    const void* x = nullptr;
+    const int* tid = nullptr;
+    float* out = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    uint64_t used = 0;
+  };
+  static constexpr int kGraphs = 16;
+  GraphEntry graphs[kGraphs];
+  uint64_t tick = 0;
+
+  int decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int n_hash, float* out,
+                   cudaGraphExec_t* exec_out);
+  void release_graphs() {
+    for (GraphEntry& g : graphs)
+      if (g.exec) {
+        cudaGraphExecDestroy(g.exec);
+        g = GraphEntry();
+      }
+    if (cap_stream) {
+      cudaStreamDestroy(cap_stream);
+      cap_stream = nullptr;
+    }
+  }
+
   int alloc(void** p, size_t n) {
     if (n == 0) n = 16;
     if (s.workspace_limit > 0 && bytes + (int64_t)n > s.workspace_limit)
@@ -138,6 +169,7 @@ struct ds4moe_handle {
     return alloc(reinterpret_cast<void**>(p), n);
   }
   void release() {
+    release_graphs();
     for (cudaEvent_t& e : ev)
       if (e) {
         cudaEventDestroy(e);
@@ -148,6 +180,46 @@ struct ds4moe_handle {
     bytes = 0;
   }
 };
+
+int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int nh, float* o,
+                                cudaGraphExec_t* exec_out) {
+  GraphEntry* hit = nullptr;
+  GraphEntry* victim = &graphs[0];
+  for (GraphEntry& g : graphs) {
+    if (g.exec && g.n == da.n_tok && g.n_hash == nh && g.x == x && g.tid == tid && g.out == o) hit = &g;
+    if (!g.exec || g.used < victim->used) victim = &g;
+  }
+  if (!hit) {
+    if (!cap_stream) DS4_CUDA(cudaStreamCreateWithFlags(&cap_stream, cudaStreamNonBlocking));
+    if (victim->exec) {
+      cudaGraphExecDestroy(victim->exec);
+      *victim = GraphEntry();
+    }
+    cudaGraph_t graph = nullptr;
+    DS4_CUDA(cudaStreamBeginCapture(cap_stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, true, cap_stream, nullptr, nullptr);
+    cudaError_t e2 = cudaStreamEndCapture(cap_stream, &graph);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();
+      return fail(DS4MOE_ERR_CUDA, "decode graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode graph instantiate: %s", cudaGetErrorString(e));
+    victim->n = da.n_tok;
+    victim->n_hash = nh;
+    victim->x = x;
+    victim->tid = tid;
+    victim->out = o;
+    victim->exec = exec;
+    hit = victim;
+  }
+  hit->used = ++tick;
+  *exec_out = hit->exec;
+  return DS4MOE_OK;
+}
 
 namespace {
 
@@ -273,6 +345,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
 
   ds4moe_handle* h = new ds4moe_handle();
   h->s = *s;
+  if (const char* ev = getenv("DS4MOE_NO_GRAPHS")) h->use_graphs = ev[0] == '0';
   const int E = s->n_experts, d = s->d, f = s->f_routed, fs = s->f_shared, K = s->top_k;
   h->mb_gu = ds4::matrix_bytes(s->fmt_gate_up, f, d);
   h->mb_d = ds4::matrix_bytes(s->fmt_down, d, f);
@@ -331,7 +404,8 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->x_stage, M * d * 2));
   DS4_TRY(h->alloc_t(&h->tid_stage, M * 4));
   DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
-  cudaError_t e = cudaMemset(h->err, 0, 4);
+  cudaError_t e = ds4::decode_prepare();
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counter, 0, 4);
@@ -401,9 +475,19 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
       decltype(mark)* m;
     } ctx{&mark};
     ds4::DecodeHooks hooks{[](void* c, const char* name) { (*static_cast<Ctx*>(c)->m)(name); }, &ctx};
-    cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, !h->profile, st, nullptr,
-                                       h->profile ? &hooks : nullptr);
-    if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    DS4_CUDA(cudaStreamIsCapturing(st, &cap));
+    if (h->profile || cap != cudaStreamCaptureStatusNone || !h->use_graphs) {
+      // direct launches (also when the caller is capturing its own graph)
+      cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, !h->profile, st, nullptr,
+                                         h->profile ? &hooks : nullptr);
+      if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    } else {
+      cudaGraphExec_t exec = nullptr;
+      int rc = h->decode_graph(da, x, token_ids, n_hash, out, &exec);
+      if (rc != DS4MOE_OK) return rc;
+      DS4_CUDA(cudaGraphLaunch(exec, st));
+    }
     h->n_phases = phase;
     h->last_stream = st;
     h->last_n = n;

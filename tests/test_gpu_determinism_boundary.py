@@ -121,3 +121,32 @@ def test_table_entries_outside_the_expert_range_are_refused():
     with pytest.raises(api.Ds4MoeError) as ei:
         moe_gpu.create(dataclasses.replace(p, hash_table=bad))
     assert ei.value.code == api.DS4MOE_ERR_INVALID_ARG
+
+
+def test_graph_replay_matches_direct_launches(monkeypatch):
+    """Decode forwards replay cached CUDA graphs; results must equal direct launches bitwise,
+    also after the graph cache has been cycled through more distinct buffers than it keeps."""
+    import torch
+
+    spec = synthetic.CONFIGS[0]
+    p = synthetic.make_problem(spec)
+    monkeypatch.setenv("DS4MOE_NO_GRAPHS", "1")
+    h_direct = moe_gpu.create(p)
+    monkeypatch.delenv("DS4MOE_NO_GRAPHS")
+    h_graph = moe_gpu.create(p)
+    try:
+        for rep in range(20):  # 20 distinct input buffers: more than the 16 cached graphs
+            xb = synthetic.activations(spec.with_(seed=100 + rep))
+            a, ia, _ = moe_gpu.forward(h_direct, p, x_bits=xb)
+            b, ib, _ = moe_gpu.forward(h_graph, p, x_bits=xb)
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)) and np.array_equal(ia, ib)
+        x = torch.from_numpy(p.x_bits.view(np.int16)).cuda()
+        out = torch.empty((spec.n_tokens, spec.d), device="cuda")
+        for _ in range(3):  # the same buffers: one cached graph replayed
+            api.ds4moe_forward(h_graph, x.data_ptr(), spec.n_tokens, out.data_ptr(), 0)
+        torch.cuda.synchronize()
+        a, _, _ = moe_gpu.forward(h_direct, p)
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), a.view(np.uint32))
+    finally:
+        api.ds4moe_destroy(h_direct)
+        api.ds4moe_destroy(h_graph)
