@@ -2,6 +2,7 @@
 // and the warp-level MMA wrapper. Device code targets sm_103a only.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -122,23 +123,6 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + 
 
 namespace ds4 {
 
-struct GemvArgs {
-  const uint8_t* w0;        // repacked stack (gate, or down)
-  const uint8_t* w1;        // repacked stack (up); unused by the down kernel
-  size_t mat_bytes;         // bytes of one expert's matrix
-  int rows;                 // output rows per matrix (f for gate/up, d for down)
-  int k;                    // reduction length (d for gate/up, f for down)
-  const int* active;        // active expert list (routed) or nullptr (shared)
-  const int* n_active;      // device count of active experts (routed)
-  const int* offsets;       // [E+1] bucketed offsets (routed)
-  const int* perm;          // bucketed position -> flat slot id t*top_k + j (routed)
-  int top_k;
-  int n_tokens;             // shared: tokens of this call
-  const __nv_bfloat16* x;   // gate/up input [n_tokens x k]
-  const float* hin;         // down input rows [pos x k] (routed: bucketed positions, shared: tokens)
-  float* out;               // gate/up: H [pos x rows]; down: Y [pos x rows]
-};
-
 // Everything the three decode kernels read and write (device pointers).
 struct DecodeArgs {
   const __nv_bfloat16* x;
@@ -193,6 +177,35 @@ int decode_max_slots();
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks);
 
+// Prefill tensor-core GEMM of one expert group (see gemm_tc.cu).
+struct GemmArgs {
+  const uint8_t* w0;       // gate (gate/up) or down stack, repacked
+  const uint8_t* w1;       // up stack (gate/up only)
+  size_t mat_bytes;        // bytes of one expert's matrix (0 for the shared expert)
+  int k;                   // reduction length
+  const int4* tiles;       // routed: device tile list (expert, first row, rows); nullptr: dense
+  const int* n_tiles;      // routed: number of tiles
+  int n_rows;              // dense: rows of the activation operand (tokens)
+  const float* inv_scale;  // gate/up: 1 / fp16 scale of each activation row
+  __half* h_out;           // gate/up output [row][ld_out] fp16
+  float* y_out;            // down output [row][ld_out] fp32
+  int ld_out;
+  int* err;                // error bits: 4 = a pipeline wait timed out, 8 = |h| beyond fp16 range
+};
+
+int gemm_tile_n();
+cudaError_t gemm_prepare();
+cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& p, int m_tiles, int n_tiles,
+                        cudaStream_t s);
+int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols);
+
+// Prefill preparation (see prefill_prep.cu).
+void launch_xprep(const __nv_bfloat16* x, int n_tok, int d, __half* xs16, float* inv_s, cudaStream_t s);
+void launch_gather(const __half* xs16, const float* inv_s, const int* perm, int n_slots, int top_k, int d,
+                   __half* xp16, float* inv_p, cudaStream_t s);
+void launch_tiles(const int* counts, const int* offsets, int n_exp, int tile_n, int4* tiles, int* n_tiles,
+                  cudaStream_t s);
+
 void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s);
 void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float* w, const float* b, int n_exp,
                           float* logits, cudaStream_t s);
@@ -201,8 +214,6 @@ void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const
 void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* counts, cudaStream_t s);
 void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* counts, int* offsets, int* active,
                            int* n_active, int* perm, int* rowof, cudaStream_t s);
-void launch_gateup(int fmt, const GemvArgs& a, int max_active, cudaStream_t s);
-void launch_down(int fmt, const GemvArgs& a, int max_active, cudaStream_t s);
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s);
 

@@ -89,10 +89,21 @@ struct ds4moe_handle {
   int* n_active = nullptr;
   int* perm = nullptr;
   int* rowof = nullptr;
-  float* H = nullptr;
-  float* Hs = nullptr;
-  float* Y = nullptr;
-  float* Ys = nullptr;
+  float* H = nullptr;   // decode: h per routed slot, fp32
+  float* Hs = nullptr;  // decode: h of the shared expert, fp32
+  float* Y = nullptr;   // prefill: down output per bucketed slot, fp32
+  float* Ys = nullptr;  // prefill: shared expert output per token, fp32
+  // prefill tensor-core path
+  __half* Xs16 = nullptr;
+  __half* Xp16 = nullptr;
+  __half* H16 = nullptr;
+  __half* Hs16 = nullptr;
+  float* inv_s = nullptr;
+  float* inv_p = nullptr;
+  int4* tiles = nullptr;
+  int* n_tiles = nullptr;
+  bool has_prefill = false;
+  CUtensorMap tm_xp, tm_xs, tm_h, tm_hs;
   int* err = nullptr;
   float* xmax = nullptr;
   float* hmax = nullptr;
@@ -388,11 +399,29 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->n_active, 4));
   DS4_TRY(h->alloc_t(&h->perm, slots * 4));
   DS4_TRY(h->alloc_t(&h->rowof, slots * 4));
-  DS4_TRY(h->alloc_t(&h->H, slots * f * 4));
-  DS4_TRY(h->alloc_t(&h->Y, slots * d * 4));
-  if (s->n_shared) {
-    DS4_TRY(h->alloc_t(&h->Hs, M * fs * 4));
-    DS4_TRY(h->alloc_t(&h->Ys, M * d * 4));
+  const size_t Md = std::min<size_t>(M, (size_t)ds4::decode_max_tokens());  // decode buffers
+  DS4_TRY(h->alloc_t(&h->H, Md * K * f * 4));
+  if (s->n_shared) DS4_TRY(h->alloc_t(&h->Hs, Md * fs * 4));
+  h->has_prefill = M > (size_t)ds4::decode_max_tokens() || slots > (size_t)ds4::decode_max_slots();
+  if (h->has_prefill) {
+    DS4_TRY(h->alloc_t(&h->Y, slots * d * 4));
+    DS4_TRY(h->alloc_t(&h->Xs16, M * d * 2));
+    DS4_TRY(h->alloc_t(&h->Xp16, slots * d * 2));
+    DS4_TRY(h->alloc_t(&h->H16, slots * f * 2));
+    DS4_TRY(h->alloc_t(&h->inv_s, M * 4));
+    DS4_TRY(h->alloc_t(&h->inv_p, slots * 4));
+    const size_t max_tiles = (slots + ds4::gemm_tile_n() - 1) / ds4::gemm_tile_n() + E;
+    DS4_TRY(h->alloc_t(&h->tiles, max_tiles * sizeof(int4)));
+    DS4_TRY(h->alloc_t(&h->n_tiles, 4));
+    if (s->n_shared) {
+      DS4_TRY(h->alloc_t(&h->Ys, M * d * 4));
+      DS4_TRY(h->alloc_t(&h->Hs16, M * fs * 2));
+    }
+    int tr = ds4::make_tmap_f16(&h->tm_xp, h->Xp16, slots, d);
+    if (!tr) tr = ds4::make_tmap_f16(&h->tm_xs, h->Xs16, M, d);
+    if (!tr) tr = ds4::make_tmap_f16(&h->tm_h, h->H16, slots, f);
+    if (!tr && s->n_shared) tr = ds4::make_tmap_f16(&h->tm_hs, h->Hs16, M, fs);
+    if (tr) DS4_TRY(fail(DS4MOE_ERR_CUDA, "tensor map encoding failed (%d)", tr));
   }
   DS4_TRY(h->alloc_t(&h->err, 4));
   DS4_TRY(h->alloc_t(&h->xmax, M * 4));
@@ -405,6 +434,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->tid_stage, M * 4));
   DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
   cudaError_t e = ds4::decode_prepare();
+  if (e == cudaSuccess) e = ds4::gemm_prepare();
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
@@ -504,26 +534,40 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   mark("bucket_count");
   ds4::launch_bucket_scatter(h->idx, n * K, E, h->counts, h->offsets, h->active, h->n_active, h->perm, h->rowof, st);
   mark("bucket_scatter");
-  const int max_active = std::min(E, n * K);
-  ds4::GemvArgs a{};
-  a.w0 = h->gate; a.w1 = h->up; a.mat_bytes = h->mb_gu; a.rows = f; a.k = d;
-  a.active = h->active; a.n_active = h->n_active; a.offsets = h->offsets; a.perm = h->perm; a.top_k = K;
-  a.n_tokens = n; a.x = xb; a.out = h->H;
-  ds4::launch_gateup(s.fmt_gate_up, a, max_active, st);
+  if (!h->has_prefill) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d needs the batched path, not sized at create", n);
+  ds4::launch_xprep(xb, n, d, h->Xs16, h->inv_s, st);
+  mark("xprep");
+  ds4::launch_gather(h->Xs16, h->inv_s, h->perm, n * K, K, d, h->Xp16, h->inv_p, st);
+  mark("gather");
+  ds4::launch_tiles(h->counts, h->offsets, E, ds4::gemm_tile_n(), h->tiles, h->n_tiles, st);
+  mark("tiles");
+  const int TN = ds4::gemm_tile_n();
+  const int routed_tiles = (n * K + TN - 1) / TN + std::min(E, n * K), dense_tiles = (n + TN - 1) / TN;
+  ds4::GemmArgs g{};
+  g.w0 = h->gate; g.w1 = h->up; g.mat_bytes = h->mb_gu; g.k = d; g.tiles = h->tiles; g.n_tiles = h->n_tiles;
+  g.inv_scale = h->inv_p; g.h_out = h->H16; g.ld_out = f; g.err = h->err;
+  cudaError_t ge = ds4::launch_gemm(s.fmt_gate_up, true, h->tm_xp, g, f / 64, routed_tiles, st);
+  if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(ge));
   mark("routed_gateup");
-  ds4::GemvArgs dn = a;
-  dn.w0 = h->down; dn.w1 = nullptr; dn.mat_bytes = h->mb_d; dn.rows = d; dn.k = f; dn.hin = h->H; dn.out = h->Y;
-  ds4::launch_down(s.fmt_down, dn, max_active, st);
+  if (s.n_shared) {
+    ds4::GemmArgs gs{};
+    gs.w0 = h->sgate; gs.w1 = h->sup; gs.k = d; gs.n_rows = n; gs.inv_scale = h->inv_s; gs.h_out = h->Hs16;
+    gs.ld_out = fs; gs.err = h->err;
+    ge = ds4::launch_gemm(s.fmt_shared, true, h->tm_xs, gs, fs / 64, dense_tiles, st);
+    if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "shared gate/up GEMM launch: %s", cudaGetErrorString(ge));
+    mark("shared_gateup");
+  }
+  ds4::GemmArgs gd{};
+  gd.w0 = h->down; gd.mat_bytes = h->mb_d; gd.k = f; gd.tiles = h->tiles; gd.n_tiles = h->n_tiles;
+  gd.y_out = h->Y; gd.ld_out = d; gd.err = h->err;
+  ge = ds4::launch_gemm(s.fmt_down, false, h->tm_h, gd, d / 128, routed_tiles, st);
+  if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "down GEMM launch: %s", cudaGetErrorString(ge));
   mark("routed_down");
   if (s.n_shared) {
-    ds4::GemvArgs sa{};
-    sa.w0 = h->sgate; sa.w1 = h->sup; sa.mat_bytes = h->mb_sgu; sa.rows = fs; sa.k = d; sa.top_k = K;
-    sa.n_tokens = n; sa.x = xb; sa.out = h->Hs;
-    ds4::launch_gateup(s.fmt_shared, sa, 1, st);
-    mark("shared_gateup");
-    ds4::GemvArgs sd = sa;
-    sd.w0 = h->sdown; sd.w1 = nullptr; sd.mat_bytes = h->mb_sd; sd.rows = d; sd.k = fs; sd.hin = h->Hs; sd.out = h->Ys;
-    ds4::launch_down(s.fmt_shared, sd, 1, st);
+    ds4::GemmArgs gsd{};
+    gsd.w0 = h->sdown; gsd.k = fs; gsd.n_rows = n; gsd.y_out = h->Ys; gsd.ld_out = d; gsd.err = h->err;
+    ge = ds4::launch_gemm(s.fmt_shared, false, h->tm_hs, gsd, d / 128, dense_tiles, st);
+    if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "shared down GEMM launch: %s", cudaGetErrorString(ge));
     mark("shared_down");
   }
   ds4::launch_combine(h->idx, h->wts, h->rowof, h->Y, s.n_shared ? h->Ys : nullptr, n, K, d, out, st);
@@ -590,8 +634,9 @@ extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n
   if (!h || n_tokens <= 0) return 0;
   if (n_tokens <= ds4::decode_max_tokens() && n_tokens * h->s.top_k <= ds4::decode_max_slots())
     return 3;  // route, gate/up, down + combine
-  // router, top-k, 2 bucketing, gate/up + down routed, the same for shared, combine
-  return 1 + 1 + 2 + 2 + (h->s.n_shared ? 2 : 0) + 1;
+  // router, top-k, 2 bucketing, activation prep + gather, tile list, routed gate/up and down GEMMs,
+  // the same for the shared expert, combine
+  return 1 + 1 + 2 + 2 + 1 + 2 + (h->s.n_shared ? 2 : 0) + 1;
 }
 
 extern "C" int ds4moe_set_profiling(ds4moe_handle* h, int32_t enable) {

@@ -1,0 +1,356 @@
+// Prefill expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+//
+// One CTA computes a 128-row x N-token tile (N <= 256, a multiple of 64) of one expert:
+//   gate/up: the 128 rows interleave 64 gate rows and the 64 up rows of the same features, so
+//            the epilogue forms h = silu(g) * u for 64 features and writes it as fp16;
+//   down:    128 rows of d, written as fp32 per bucketed slot for the fixed-order combine.
+// Warp roles (10 warps):
+//   warp 0     producer: bulk-copies the packed weight units of each K unit (256 k for Q2_K,
+//              128 k for Q8_0) and TMA-loads the activation tile (fp16, 128-byte swizzle) of
+//              each 64-wide K stage;
+//   warp 1     allocates TMEM; one thread issues the tcgen05.mma of every stage;
+//   warps 2-9  dequantize: each turns one 16-row packed unit into fp16 weights in registers
+//              (exact small-integer quants, fp16 FMA with the sub-block scale and min) and
+//              writes them with stmatrix straight into the swizzled A tile; afterwards they run
+//              the epilogue from TMEM (tcgen05.ld).
+// Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
+// unwinds instead of hanging.
+#include <cudaTypedefs.h>
+
+#include "tc_ptx.cuh"
+
+namespace ds4 {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 3, RAWS = 2;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
+constexpr int RAW_BYTES = 8 * kQ80UnitBytes;    // 17408: eight 16-row units of either format
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = (2 + kDeqWarps) * 32;  // 320
+constexpr int TMEM_COLS = 256;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
+constexpr int N_BARS = 3 * STAGES + 2 * RAWS + 1;
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
+constexpr int GBUF_BYTES = 2 * 64 * 16 * 4;  // per epilogue group: 64 gate rows x 16 columns fp32
+constexpr int SMEM_BYTES = OFF_GBUF + GBUF_BYTES + 1024;  // + alignment slack
+
+struct Bars {
+  uint64_t* full_a;   // [STAGES] dequant warps -> MMA
+  uint64_t* full_b;   // [STAGES] activation TMA -> MMA
+  uint64_t* empty;    // [STAGES] MMA commit -> producer, dequant
+  uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
+  uint64_t* raw_empty;  // [RAWS] dequant -> producer
+  uint64_t* acc_full;   // MMA -> epilogue
+};
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// stmatrix row address of this lane for the 16x16 block (row group rg16 of the tile, 16-k
+// sub-block sb of the 64-k stage) in the 128-byte swizzled A tile.
+__device__ __forceinline__ uint32_t a_row_addr(uint32_t a_base, int rg16, int sb) {
+  const int lane = threadIdx.x & 31, j = lane >> 3, q = lane & 7;
+  const int row = 16 * rg16 + q + 8 * (j & 1);
+  const int kc = 2 * sb + (j >> 1);  // 16-byte chunk of the 128-byte row
+  return a_base + (row >> 3) * 1024 + (row & 7) * 128 + ((kc ^ (row & 7)) << 4);
+}
+
+// Dequantize the 16 rows x 64 k of one Q2_K unit that fall in K stage su (0..3) and store them.
+__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int rg16) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  const int c = su >> 1, i0 = (su & 1) * 4;
+  const uint4 qw = lds128(unit + c * 512 + 16 * lane);
+  const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
+  const uint32_t sca = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
+  const uint32_t scb = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
+  const __half2 d2 = u2h(prmt(dd0, dd1, 0x5410u));    // (d of row g, d of row g+8)
+  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));   // (dmin of row g, dmin of row g+8)
+  const __half2 k1024 = __float2half2_rn(1024.f);
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = i0 + ii;
+    const uint32_t sc = (ii < 2 ? sca : scb) >> (8 * (ii & 1));
+    // (s_g, s_g8) and (m_g, m_g8) as exact fp16 integers through the 1024 + x encoding
+    const __half2 s2 = __hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024);
+    const __half2 m2 = __hsub2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), k1024);
+    const __half2 ds = __hmul2(s2, d2);             // (d*s) of rows g, g+8, rounded once to fp16
+    const __half2 ndm = __hneg2(__hmul2(m2, dm2));  // -(dmin*m)
+    const __half2 ds_g = u2h(prmt(h2u(ds), 0u, 0x1010u)), ds_h = u2h(prmt(h2u(ds), 0u, 0x3232u));
+    const __half2 nm_g = u2h(prmt(h2u(ndm), 0u, 0x1010u)), nm_h = u2h(prmt(h2u(ndm), 0u, 0x3232u));
+    uint32_t a[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const __half2 q = __hsub2(u2h(((w[r] >> (2 * i)) & 0x00030003u) | 0x64006400u), k1024);
+      a[r] = h2u(__hfma2(q, (r & 1) ? ds_h : ds_g, (r & 1) ? nm_h : nm_g));
+    }
+    stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
+  }
+}
+
+// Dequantize the 16 rows x 64 k of one Q8_0 unit (128 k) that fall in K stage su (0..1).
+__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int rg16) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  const __half2 k1152 = __float2half2_rn(1152.f);
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = 4 * su + ii;  // MMA index (16-k sub-block) inside the unit
+    const uint4 v = lds128(unit + 512 * (i >> 1) + 16 * lane);
+    const uint32_t wa = (i & 1) ? v.z : v.x, wb = (i & 1) ? v.w : v.y;
+    const uint32_t scw = lds32(unit + kQ80ScOff + 4 * (4 * g + (i >> 1)));  // block i/2, rows g, g+8
+    const __half2 s_g = u2h(prmt(scw, 0u, 0x1010u)), s_h = u2h(prmt(scw, 0u, 0x3232u));
+    const uint32_t raw[4] = {prmt(wa, 0x64u, 0x4140u), prmt(wa, 0x64u, 0x4342u), prmt(wb, 0x64u, 0x4140u),
+                             prmt(wb, 0x64u, 0x4342u)};  // fp16 1024 + u, u = q + 128
+    uint32_t a[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? s_h : s_g));
+    stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
+  }
+}
+
+template <int FMT, bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
+                                                                      GemmArgs p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- tile
+  int expert, row0, rows;
+  if (p.tiles) {
+    if ((int)blockIdx.y >= *p.n_tiles) return;
+    const int4 t = p.tiles[blockIdx.y];
+    expert = t.x; row0 = t.y; rows = t.z;
+  } else {
+    expert = -1;
+    row0 = blockIdx.y * BN;
+    rows = min(BN, p.n_rows - row0);
+  }
+  if (rows <= 0) return;
+  const int nbox = (rows + BOX_ROWS - 1) / BOX_ROWS;
+  const int n = nbox * BOX_ROWS;  // MMA N
+  const int mt = blockIdx.x;
+  constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT);
+  const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
+  const size_t eoff = expert >= 0 ? (size_t)expert * p.mat_bytes : 0;
+  const uint8_t* src0;
+  const uint8_t* src1;
+  uint32_t raw_copy;  // bytes of each of the (one or two) weight copies per K unit
+  if (GATEUP) {  // 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63
+    src0 = p.w0 + eoff;
+    src1 = p.w1 + eoff;
+    raw_copy = 4 * UB;
+  } else {  // 128 rows of d
+    src0 = p.w0 + eoff;
+    src1 = nullptr;
+    raw_copy = 8 * UB;
+  }
+  const int rg0 = GATEUP ? 4 * mt : 8 * mt;  // first 16-row group of the tile's rows
+
+  Bars b;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  b.full_a = bars;
+  b.full_b = bars + STAGES;
+  b.empty = bars + 2 * STAGES;
+  b.raw_full = bars + 3 * STAGES;
+  b.raw_empty = bars + 3 * STAGES + RAWS;
+  b.acc_full = bars + 3 * STAGES + 2 * RAWS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  float* gbuf = reinterpret_cast<float*>(smem + OFF_GBUF);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&b.full_a[s], kDeqWarps);
+      mbar_init(&b.full_b[s], 1);
+      mbar_init(&b.empty[s], 1);
+    }
+    for (int r = 0; r < RAWS; ++r) {
+      mbar_init(&b.raw_full[r], 1);
+      mbar_init(&b.raw_empty[r], kDeqWarps);
+    }
+    mbar_init(b.acc_full, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int s = 0; s < n_stages; ++s) {
+        if (s % kpu == 0) {
+          const int u = s / kpu, rs = u % RAWS;
+          if (!mbar_wait(&b.raw_empty[rs], ((u / RAWS) & 1) ^ 1, abort_flag, p.err)) break;
+          unsigned char* dst = smem + OFF_RAW + rs * RAW_BYTES;
+          mbar_expect_tx(&b.raw_full[rs], GATEUP ? 2 * raw_copy : raw_copy);
+          bulk_load(dst, src0 + unit_offset(rg0, u, n_kb, UB), raw_copy, &b.raw_full[rs]);
+          if (GATEUP) bulk_load(dst + raw_copy, src1 + unit_offset(rg0, u, n_kb, UB), raw_copy, &b.raw_full[rs]);
+        }
+        const int st = s % STAGES;
+        if (!mbar_wait(&b.empty[st], ((s / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+        unsigned char* bdst = smem + OFF_B + st * B_BYTES;
+        mbar_expect_tx(&b.full_b[st], nbox * BOX_ROWS * BK * 2);
+        for (int bx = 0; bx < nbox; ++bx)
+          tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, s * BK, row0 + bx * BOX_ROWS, &b.full_b[st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(BM, n);
+      for (int s = 0; s < n_stages; ++s) {
+        const int st = s % STAGES;
+        const uint32_t par = (s / STAGES) & 1;
+        if (!mbar_wait(&b.full_a[st], par, abort_flag, p.err)) break;
+        if (!mbar_wait(&b.full_b[st], par, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(su32(smem + OFF_A + st * A_BYTES));
+        const uint64_t bd = sw128_desc(su32(smem + OFF_B + st * B_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
+          tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+        tc_commit(&b.empty[st]);
+      }
+      tc_commit(b.acc_full);
+    }
+  } else {
+    // ------------------------------------------------------------------ dequant
+    const int dw = warp - 2;  // 16-row group of the tile this warp writes
+    for (int s = 0; s < n_stages; ++s) {
+      const int u = s / kpu, rs = u % RAWS, st = s % STAGES, su = s % kpu;
+      if (su == 0 && !mbar_wait(&b.raw_full[rs], (u / RAWS) & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(&b.empty[st], ((s / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+      const uint32_t unit = su32(smem + OFF_RAW + rs * RAW_BYTES + dw * UB);
+      const uint32_t a_base = su32(smem + OFF_A + st * A_BYTES);
+      if (FMT == FMT_Q2_K)
+        deq_q2k(unit, su, a_base, dw);
+      else
+        deq_q80(unit, su, a_base, dw);
+      fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&b.full_a[st]);
+        if (su == kpu - 1) mbar_arrive(&b.raw_empty[rs]);
+      }
+    }
+    // ------------------------------------------------------------------ epilogue
+    if (mbar_wait(b.acc_full, 0, abort_flag, p.err)) {
+      tc_fence_after();
+      const int grp = (warp - 2) >> 2;        // two groups of four warps split the columns
+      const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+      const int row = 32 * quad + lane;       // tile row = TMEM lane
+      const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
+      float* gb = gbuf + grp * 64 * 16;
+      for (int c0 = 16 * grp; c0 < n; c0 += 32) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c0, r);
+        tmem_ld_wait();
+        if (GATEUP) {
+          if (quad < 2) {  // gate rows: hand g to the up warps through shared memory
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gb[row * 16 + j] = __uint_as_float(r[j]);
+          }
+          named_bar(1 + grp, 128);
+          if (quad >= 2) {
+            const int feat = 64 * mt + row - 64;
+            unsigned bad = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < rows) {
+                const float inv = p.inv_scale[row0 + col];
+                const float h = silu_mul(gb[(row - 64) * 16 + j] * inv, __uint_as_float(r[j]) * inv);
+                bad |= !(fabsf(h) <= 65504.f);
+                p.h_out[(size_t)(row0 + col) * p.ld_out + feat] = __float2half_rn(h);
+              }
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 8);
+          }
+          named_bar(1 + grp, 128);
+        } else {
+          const int drow = 128 * mt + row;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < rows) p.y_out[(size_t)(row0 + col) * p.ld_out + drow] = __uint_as_float(r[j]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int FMT, bool GATEUP>
+cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
+  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, SMEM_BYTES, s>>>(tm, p);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool GATEUP>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
+}
+
+}  // namespace
+
+int gemm_tile_n() { return BN; }
+
+cudaError_t gemm_prepare() {
+  cudaError_t e = prepare_one<FMT_Q2_K, true>();
+  if (e == cudaSuccess) e = prepare_one<FMT_Q2_K, false>();
+  if (e == cudaSuccess) e = prepare_one<FMT_Q8_0, true>();
+  if (e == cudaSuccess) e = prepare_one<FMT_Q8_0, false>();
+  return e;
+}
+
+cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& p, int m_tiles, int n_tiles,
+                        cudaStream_t s) {
+  const dim3 grid(m_tiles, n_tiles);
+  if (fmt == FMT_Q2_K) return gateup ? launch_one<FMT_Q2_K, true>(tm, p, grid, s) : launch_one<FMT_Q2_K, false>(tm, p, grid, s);
+  return gateup ? launch_one<FMT_Q8_0, true>(tm, p, grid, s) : launch_one<FMT_Q8_0, false>(tm, p, grid, s);
+}
+
+// fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x 64 rows with
+// the 128-byte swizzle (the K-major canonical layout of the MMA's B operand).
+int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return -1;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {BK, BOX_ROWS};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+}  // namespace ds4
