@@ -326,6 +326,42 @@ int check_table(const int* dev_table, size_t n, int n_exp) {
   return DS4MOE_OK;
 }
 
+// The batched path dequantizes Q2_K weights in fp16 as q * 2^-16 times 2^16 d s: every super-
+// block needs 15 * 2^16 * |d| inside the fp16 range, i.e. |d| < 0.0666 (typical d are ~1e-3).
+int check_q2k_scales(ds4moe_handle* h) {
+  const ds4moe_shapes& s = h->s;
+  const uint8_t* stacks[4] = {nullptr, nullptr, nullptr, nullptr};
+  size_t bytes[4] = {0, 0, 0, 0};
+  if (s.fmt_gate_up == DS4MOE_FMT_Q2_K) {
+    stacks[0] = h->gate; bytes[0] = h->mb_gu * s.n_experts;
+    stacks[1] = h->up; bytes[1] = h->mb_gu * s.n_experts;
+  }
+  if (s.fmt_down == DS4MOE_FMT_Q2_K) { stacks[2] = h->down; bytes[2] = h->mb_d * s.n_experts; }
+  unsigned* dmax = nullptr;
+  DS4_CUDA(cudaMalloc(&dmax, 4));
+  cudaError_t e = cudaMemset(dmax, 0, 4);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    if (stacks[i]) {
+      ds4::launch_q2k_dmax(stacks[i], bytes[i], dmax, 0);
+      e = cudaGetLastError();
+    }
+  if (s.n_shared && s.fmt_shared == DS4MOE_FMT_Q2_K && e == cudaSuccess) {
+    ds4::launch_q2k_dmax(h->sgate, h->mb_sgu, dmax, 0);
+    ds4::launch_q2k_dmax(h->sup, h->mb_sgu, dmax, 0);
+    ds4::launch_q2k_dmax(h->sdown, h->mb_sd, dmax, 0);
+    e = cudaGetLastError();
+  }
+  unsigned bits = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bits, dmax, 4, cudaMemcpyDeviceToHost);
+  cudaFree(dmax);
+  if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "Q2_K scale check: %s", cudaGetErrorString(e));
+  float d;
+  memcpy(&d, &bits, 4);
+  if (!(d * 15.f * 65536.f < 65504.f))
+    return fail(DS4MOE_ERR_UNSUPPORTED_FORMAT, "Q2_K super-block scale |d| = %g: the batched path needs |d| < 0.0666", d);
+  return DS4MOE_OK;
+}
+
 #define DS4_TRY(call)          \
   do {                         \
     int rc_ = (call);          \
@@ -422,6 +458,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
     if (!tr) tr = ds4::make_tmap_f16(&h->tm_h, h->H16, slots, f);
     if (!tr && s->n_shared) tr = ds4::make_tmap_f16(&h->tm_hs, h->Hs16, M, fs);
     if (tr) DS4_TRY(fail(DS4MOE_ERR_CUDA, "tensor map encoding failed (%d)", tr));
+    DS4_TRY(check_q2k_scales(h));
   }
   DS4_TRY(h->alloc_t(&h->err, 4));
   DS4_TRY(h->alloc_t(&h->xmax, M * 4));

@@ -25,29 +25,38 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 3, RAWS = 2;
+constexpr int A_STAGES = 2;  // dequantized weight tiles (written on chip: little latency to hide)
+constexpr int B_STAGES = 4;  // activation tiles (TMA from L2/HBM)
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
-constexpr int RAW_BYTES = 8 * kQ80UnitBytes;    // 17408: eight 16-row units of either format
 constexpr int kDeqWarps = 8;
 constexpr int kThreads = (2 + kDeqWarps) * 32;  // 320
 constexpr int TMEM_COLS = 256;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
-constexpr int N_BARS = 3 * STAGES + 2 * RAWS + 1;
-constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
-constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
-constexpr int GBUF_BYTES = 2 * 64 * 16 * 4;  // per epilogue group: 64 gate rows x 16 columns fp32
-constexpr int SMEM_BYTES = OFF_GBUF + GBUF_BYTES + 1024;  // + alignment slack
+// Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
+// Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
+template <int FMT>
+struct Cfg {
+  static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);
+  static constexpr int RAWS = FMT == FMT_Q2_K ? 4 : 3;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + A_STAGES * A_BYTES;
+  static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
+  static constexpr int N_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * RAWS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int GBUF_BYTES = 2 * 64 * 16 * 4;  // per epilogue group: 16 columns x 64 gate rows fp32
+  static constexpr int SMEM_BYTES = OFF_GBUF + GBUF_BYTES + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 struct Bars {
-  uint64_t* full_a;   // [STAGES] dequant warps -> MMA
-  uint64_t* full_b;   // [STAGES] activation TMA -> MMA
-  uint64_t* empty;    // [STAGES] MMA commit -> producer, dequant
+  uint64_t* a_full;     // [A_STAGES] dequant warps -> MMA
+  uint64_t* a_empty;    // [A_STAGES] MMA commit -> dequant
+  uint64_t* b_full;     // [B_STAGES] activation TMA -> MMA
+  uint64_t* b_empty;    // [B_STAGES] MMA commit -> producer
   uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
   uint64_t* raw_empty;  // [RAWS] dequant -> producer
   uint64_t* acc_full;   // MMA -> epilogue
@@ -74,7 +83,10 @@ __device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, 
   const uint32_t sca = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
   const uint32_t scb = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
   const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
-  const __half2 d2 = u2h(prmt(dd0, dd1, 0x5410u));    // (d of row g, d of row g+8)
+  // (d of row g, d of row g+8) times 2^16: exact (only the exponent changes); create refuses
+  // super-blocks whose d * 15 * 2^16 would leave the fp16 range
+  const __half2 k256 = __float2half2_rn(256.f);
+  const __half2 d2 = __hmul2(__hmul2(u2h(prmt(dd0, dd1, 0x5410u)), k256), k256);
   const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));   // (dmin of row g, dmin of row g+8)
   const __half2 k1024 = __float2half2_rn(1024.f);
 #pragma unroll
@@ -84,15 +96,17 @@ __device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, 
     // (s_g, s_g8) and (m_g, m_g8) as exact fp16 integers through the 1024 + x encoding
     const __half2 s2 = __hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024);
     const __half2 m2 = __hsub2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), k1024);
-    const __half2 ds = __hmul2(s2, d2);             // (d*s) of rows g, g+8, rounded once to fp16
+    const __half2 ds = __hmul2(s2, d2);             // 2^16 * d*s of rows g, g+8, rounded once to fp16
     const __half2 ndm = __hneg2(__hmul2(m2, dm2));  // -(dmin*m)
     const __half2 ds_g = u2h(prmt(h2u(ds), 0u, 0x1010u)), ds_h = u2h(prmt(h2u(ds), 0u, 0x3232u));
     const __half2 nm_g = u2h(prmt(h2u(ndm), 0u, 0x1010u)), nm_h = u2h(prmt(h2u(ndm), 0u, 0x3232u));
     uint32_t a[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const __half2 q = __hsub2(u2h(((w[r] >> (2 * i)) & 0x00030003u) | 0x64006400u), k1024);
-      a[r] = h2u(__hfma2(q, (r & 1) ? ds_h : ds_g, (r & 1) ? nm_h : nm_g));
+      // the quant pair moved to mantissa bits 8-9: the exact fp16 subnormal q * 2^-16, so one
+      // FMA with 2^16 d s gives d s q - dmin m with a single rounding
+      const uint32_t qb = (i < 4 ? (w[r] << (8 - 2 * i)) : (w[r] >> (2 * i - 8))) & 0x03000300u;
+      a[r] = h2u(__hfma2(u2h(qb), (r & 1) ? ds_h : ds_g, (r & 1) ? nm_h : nm_g));
     }
     stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
   }
@@ -121,6 +135,7 @@ __device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, 
 template <int FMT, bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
                                                                       GemmArgs p) {
+  using C = Cfg<FMT>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,40 +154,36 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   const int nbox = (rows + BOX_ROWS - 1) / BOX_ROWS;
   const int n = nbox * BOX_ROWS;  // MMA N
   const int mt = blockIdx.x;
-  constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT);
+  constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
   const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
   const size_t eoff = expert >= 0 ? (size_t)expert * p.mat_bytes : 0;
-  const uint8_t* src0;
-  const uint8_t* src1;
-  uint32_t raw_copy;  // bytes of each of the (one or two) weight copies per K unit
-  if (GATEUP) {  // 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63
-    src0 = p.w0 + eoff;
-    src1 = p.w1 + eoff;
-    raw_copy = 4 * UB;
-  } else {  // 128 rows of d
-    src0 = p.w0 + eoff;
-    src1 = nullptr;
-    raw_copy = 8 * UB;
-  }
+  const uint8_t* src0 = p.w0 + eoff;
+  const uint8_t* src1 = GATEUP ? p.w1 + eoff : nullptr;
+  // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
+  const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
   const int rg0 = GATEUP ? 4 * mt : 8 * mt;  // first 16-row group of the tile's rows
 
   Bars b;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  b.full_a = bars;
-  b.full_b = bars + STAGES;
-  b.empty = bars + 2 * STAGES;
-  b.raw_full = bars + 3 * STAGES;
-  b.raw_empty = bars + 3 * STAGES + RAWS;
-  b.acc_full = bars + 3 * STAGES + 2 * RAWS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  float* gbuf = reinterpret_cast<float*>(smem + OFF_GBUF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  b.a_full = bars;
+  b.a_empty = bars + A_STAGES;
+  b.b_full = bars + 2 * A_STAGES;
+  b.b_empty = bars + 2 * A_STAGES + B_STAGES;
+  b.raw_full = bars + 2 * A_STAGES + 2 * B_STAGES;
+  b.raw_empty = b.raw_full + RAWS;
+  b.acc_full = b.raw_empty + RAWS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* gbuf = reinterpret_cast<float*>(smem + C::OFF_GBUF);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&b.full_a[s], kDeqWarps);
-      mbar_init(&b.full_b[s], 1);
-      mbar_init(&b.empty[s], 1);
+    for (int i = 0; i < A_STAGES; ++i) {
+      mbar_init(&b.a_full[i], kDeqWarps);
+      mbar_init(&b.a_empty[i], 1);
+    }
+    for (int i = 0; i < B_STAGES; ++i) {
+      mbar_init(&b.b_full[i], 1);
+      mbar_init(&b.b_empty[i], 1);
     }
     for (int r = 0; r < RAWS; ++r) {
       mbar_init(&b.raw_full[r], 1);
@@ -194,21 +205,37 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int s = 0; s < n_stages; ++s) {
-        if (s % kpu == 0) {
-          const int u = s / kpu, rs = u % RAWS;
-          if (!mbar_wait(&b.raw_empty[rs], ((u / RAWS) & 1) ^ 1, abort_flag, p.err)) break;
-          unsigned char* dst = smem + OFF_RAW + rs * RAW_BYTES;
+      // Two independent streams, each issued as soon as its buffer is free: the weight units (up
+      // to RAWS K units ahead of the dequant warps) and the activation tiles (up to B_STAGES
+      // stages ahead of the MMA). Neither waits for the other.
+      int sB = 0, uN = 0;
+      long long last = clock64();
+      while ((sB < n_stages || uN < n_kb) && !*abort_flag) {
+        bool progressed = false;
+        if (uN < n_kb && mbar_try(&b.raw_empty[uN % RAWS], ((uN / RAWS) & 1) ^ 1)) {
+          const int rs = uN % RAWS;
+          unsigned char* dst = smem + C::OFF_RAW + rs * C::RAW_BYTES;
           mbar_expect_tx(&b.raw_full[rs], GATEUP ? 2 * raw_copy : raw_copy);
-          bulk_load(dst, src0 + unit_offset(rg0, u, n_kb, UB), raw_copy, &b.raw_full[rs]);
-          if (GATEUP) bulk_load(dst + raw_copy, src1 + unit_offset(rg0, u, n_kb, UB), raw_copy, &b.raw_full[rs]);
+          bulk_load(dst, src0 + unit_offset(rg0, uN, n_kb, UB), raw_copy, &b.raw_full[rs]);
+          if (GATEUP) bulk_load(dst + raw_copy, src1 + unit_offset(rg0, uN, n_kb, UB), raw_copy, &b.raw_full[rs]);
+          ++uN;
+          progressed = true;
         }
-        const int st = s % STAGES;
-        if (!mbar_wait(&b.empty[st], ((s / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
-        unsigned char* bdst = smem + OFF_B + st * B_BYTES;
-        mbar_expect_tx(&b.full_b[st], nbox * BOX_ROWS * BK * 2);
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, s * BK, row0 + bx * BOX_ROWS, &b.full_b[st]);
+        if (sB < n_stages && mbar_try(&b.b_empty[sB % B_STAGES], ((sB / B_STAGES) & 1) ^ 1)) {
+          const int sb = sB % B_STAGES;
+          unsigned char* bdst = smem + C::OFF_B + sb * B_BYTES;
+          mbar_expect_tx(&b.b_full[sb], nbox * BOX_ROWS * BK * 2);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, row0 + bx * BOX_ROWS, &b.b_full[sb]);
+          ++sB;
+          progressed = true;
+        }
+        if (progressed) {
+          last = clock64();
+        } else if (clock64() - last > kTimeoutCycles) {
+          *abort_flag = 1;
+          atomicOr(p.err, 4);
+        }
       }
     }
   } else if (warp == 1) {
@@ -216,17 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(BM, n);
       for (int s = 0; s < n_stages; ++s) {
-        const int st = s % STAGES;
-        const uint32_t par = (s / STAGES) & 1;
-        if (!mbar_wait(&b.full_a[st], par, abort_flag, p.err)) break;
-        if (!mbar_wait(&b.full_b[st], par, abort_flag, p.err)) break;
+        const int sa = s % A_STAGES, sb = s % B_STAGES;
+        if (!mbar_wait(&b.a_full[sa], (s / A_STAGES) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&b.b_full[sb], (s / B_STAGES) & 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint64_t ad = sw128_desc(su32(smem + OFF_A + st * A_BYTES));
-        const uint64_t bd = sw128_desc(su32(smem + OFF_B + st * B_BYTES));
+        const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + sa * A_BYTES));
+        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + sb * B_BYTES));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
           tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-        tc_commit(&b.empty[st]);
+        tc_commit(&b.a_empty[sa]);
+        tc_commit(&b.b_empty[sb]);
       }
       tc_commit(b.acc_full);
     }
@@ -234,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     // ------------------------------------------------------------------ dequant
     const int dw = warp - 2;  // 16-row group of the tile this warp writes
     for (int s = 0; s < n_stages; ++s) {
-      const int u = s / kpu, rs = u % RAWS, st = s % STAGES, su = s % kpu;
+      const int u = s / kpu, rs = u % RAWS, sa = s % A_STAGES, su = s % kpu;
       if (su == 0 && !mbar_wait(&b.raw_full[rs], (u / RAWS) & 1, abort_flag, p.err)) break;
-      if (!mbar_wait(&b.empty[st], ((s / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
-      const uint32_t unit = su32(smem + OFF_RAW + rs * RAW_BYTES + dw * UB);
-      const uint32_t a_base = su32(smem + OFF_A + st * A_BYTES);
+      if (!mbar_wait(&b.a_empty[sa], ((s / A_STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+      const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + dw * UB);
+      const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
       if (FMT == FMT_Q2_K)
         deq_q2k(unit, su, a_base, dw);
       else
@@ -246,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&b.full_a[st]);
+        mbar_arrive(&b.a_full[sa]);
         if (su == kpu - 1) mbar_arrive(&b.raw_empty[rs]);
       }
     }
@@ -257,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       const int quad = warp & 3;              // TMEM lane quadrant this warp may access
       const int row = 32 * quad + lane;       // tile row = TMEM lane
       const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-      float* gb = gbuf + grp * 64 * 16;
+      float* gb = gbuf + grp * 64 * 16;       // [column][gate row]: conflict-free by lane
       for (int c0 = 16 * grp; c0 < n; c0 += 32) {
         uint32_t r[16];
         tmem_ld16(taddr + c0, r);
@@ -265,18 +292,20 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         if (GATEUP) {
           if (quad < 2) {  // gate rows: hand g to the up warps through shared memory
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gb[row * 16 + j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j) gb[j * 64 + row] = __uint_as_float(r[j]);
           }
           named_bar(1 + grp, 128);
           if (quad >= 2) {
             const int feat = 64 * mt + row - 64;
+            float inv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) inv[j] = c0 + j < rows ? __ldg(p.inv_scale + row0 + c0 + j) : 0.f;
             unsigned bad = 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
               if (col < rows) {
-                const float inv = p.inv_scale[row0 + col];
-                const float h = silu_mul(gb[(row - 64) * 16 + j] * inv, __uint_as_float(r[j]) * inv);
+                const float h = silu_mul(gb[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
                 bad |= !(fabsf(h) <= 65504.f);
                 p.h_out[(size_t)(row0 + col) * p.ld_out + feat] = __float2half_rn(h);
               }
@@ -302,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
 template <int FMT, bool GATEUP>
 cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
-  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, SMEM_BYTES, s>>>(tm, p);
+  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm, p);
   return cudaGetLastError();
 }
 
 template <int FMT, bool GATEUP>
 cudaError_t prepare_one() {
   return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
+                              Cfg<FMT>::SMEM_BYTES);
 }
 
 }  // namespace

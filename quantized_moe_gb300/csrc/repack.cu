@@ -87,7 +87,21 @@ __global__ void repack_q80_kernel(const uint8_t* __restrict__ src, uint8_t* __re
   }
 }
 
+// Largest |d| of all super-blocks of a repacked Q2_K stack (as float bits, for atomicMax).
+__global__ void q2k_dmax_kernel(const uint8_t* __restrict__ packed, size_t n_units, unsigned* __restrict__ out) {
+  unsigned m = 0;
+  for (size_t u = blockIdx.x * (size_t)blockDim.x + threadIdx.x; u < n_units * 16; u += (size_t)gridDim.x * blockDim.x) {
+    const __half dh = *reinterpret_cast<const __half*>(packed + (u / 16) * kQ2kUnitBytes + kQ2kDdOff + 4 * (u % 16));
+    m = max(m, __float_as_uint(fabsf(__half2float(dh))));
+  }
+  atomicMax(out, m);
+}
+
 }  // namespace
+
+void launch_q2k_dmax(const uint8_t* packed, size_t bytes, unsigned* out, cudaStream_t s) {
+  q2k_dmax_kernel<<<152 * 4, 256, 0, s>>>(packed, bytes / kQ2kUnitBytes, out);
+}
 
 void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s) {
   const int threads = 256, blocks = 152 * 8;

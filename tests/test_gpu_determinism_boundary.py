@@ -150,3 +150,18 @@ def test_graph_replay_matches_direct_launches(monkeypatch):
     finally:
         api.ds4moe_destroy(h_direct)
         api.ds4moe_destroy(h_graph)
+
+
+def test_q2k_scale_beyond_fp16_dequant_range_is_refused():
+    """The batched path dequantizes Q2_K in fp16 (q * 2^-16 times 2^16 d s): a super-block
+    scale d >= 1/15 would overflow, so create refuses it by name (decode-only handles accept it)."""
+    p = synthetic.make_problem(SMALL_MIX)
+    gate = np.stack([p.gate[e] for e in range(SMALL_MIX.n_experts)]).copy()
+    blk = gate.reshape(SMALL_MIX.n_experts, SMALL_MIX.f, -1, 84)
+    blk[3, 5, 1, 80:82] = np.frombuffer(np.float16(0.1).tobytes(), np.uint8)
+    q = dataclasses.replace(p, gate=gate)
+    with pytest.raises(api.Ds4MoeError) as ei:
+        moe_gpu.create(q, max_tokens=64)
+    assert ei.value.code == api.DS4MOE_ERR_UNSUPPORTED_FORMAT
+    h = moe_gpu.create(q, max_tokens=4)  # decode path only: no fp16 dequant, accepted
+    api.ds4moe_destroy(h)
