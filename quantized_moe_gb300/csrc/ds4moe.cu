@@ -71,6 +71,7 @@ struct ds4moe_handle {
   // weights
   float* router_w = nullptr;
   float* router_b = nullptr;
+  __nv_bfloat16* router_w3 = nullptr;  // batched path: the router weights as three bf16 parts
   uint8_t* gate = nullptr;
   uint8_t* up = nullptr;
   uint8_t* down = nullptr;
@@ -459,6 +460,8 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
     if (!tr && s->n_shared) tr = ds4::make_tmap_f16(&h->tm_hs, h->Hs16, M, fs);
     if (tr) DS4_TRY(fail(DS4MOE_ERR_CUDA, "tensor map encoding failed (%d)", tr));
     DS4_TRY(check_q2k_scales(h));
+    DS4_TRY(h->alloc_t(&h->router_w3, (size_t)3 * E * d * 2));
+    ds4::launch_router_split(h->router_w, (size_t)E * d, h->router_w3, 0);
   }
   DS4_TRY(h->alloc_t(&h->err, 4));
   DS4_TRY(h->alloc_t(&h->xmax, M * 4));
@@ -561,7 +564,7 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
     return DS4MOE_OK;
   }
   if (n_learned > 0) {
-    ds4::launch_router_logits(xb + (size_t)n_hash * d, n_learned, d, h->router_w, h->router_b, E, h->logits, st);
+    ds4::launch_router_tc(xb + (size_t)n_hash * d, n_learned, d, h->router_w3, h->router_b, E, h->logits, st);
     mark("router_logits");
   }
   DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));

@@ -1,0 +1,140 @@
+// Batched router logits on the tensor cores with fp32 accuracy.
+//
+// The fp32 router weights are split once, at create time, into three bf16 parts
+// w = w_hi + w_mid + w_lo (8 + 8 + 8 significand bits cover all 24 of fp32). The activations are
+// bf16 already, so every product x * w_part is exact in fp32, and an m16n8k16 bf16 MMA with an
+// fp32 accumulator over the three parts gives the fp32 dot product: the same accuracy as fp32
+// FMAs on the CUDA cores, at tensor-core throughput.
+//
+// CTA = 64 tokens x 64 experts, 4 warps (16 tokens each, all 64 experts); K staged through
+// shared memory 32 at a time, double-buffered with cp.async.
+#include "common.cuh"
+
+namespace ds4 {
+namespace {
+
+constexpr int TT = 64, TE = 64, KS = 32;
+constexpr int PAD = 8;  // bf16 elements of padding per shared row (keeps ldmatrix conflict-free)
+constexpr int LDS = KS + PAD;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool pred) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int sz = pred ? 16 : 0;  // zero-fill rows past the end
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(sz) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// w3: [3][E][d] bf16 parts of the router weights
+__global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
+                                                        const __nv_bfloat16* __restrict__ w3, const float* __restrict__ b,
+                                                        int n_exp, float* __restrict__ logits) {
+  __shared__ __align__(16) __nv_bfloat16 xs[2][TT][LDS];
+  __shared__ __align__(16) __nv_bfloat16 ws[2][3][TE][LDS];
+  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * TE;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t plane = (size_t)n_exp * d;
+  auto stage = [&](int buf, int k0) {
+    // 64 rows x 32 k = 256 chunks of 16 bytes for x, 3 x 256 for the weight parts; 128 threads
+    for (int c = threadIdx.x; c < 4 * TT * (KS / 8); c += 128) {
+      const int which = c / (TT * (KS / 8)), r = (c / (KS / 8)) % TT, kc = c % (KS / 8);
+      if (which == 0) {
+        const int t = t0 + r;
+        cp_async16(&xs[buf][r][kc * 8], x + (size_t)min(t, n_tok - 1) * d + k0 + kc * 8, t < n_tok);
+      } else {
+        const int e = e0 + r;
+        cp_async16(&ws[buf][which - 1][r][kc * 8], w3 + (which - 1) * plane + (size_t)min(e, n_exp - 1) * d + k0 + kc * 8,
+                   e < n_exp);
+      }
+    }
+    cp_async_commit();
+  };
+  float acc[TE / 8][4];
+#pragma unroll
+  for (int j = 0; j < TE / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  const int n_k = d / KS;
+  stage(0, 0);
+  for (int ks = 0; ks < n_k; ++ks) {
+    const int buf = ks & 1;
+    if (ks + 1 < n_k) {
+      stage(buf ^ 1, (ks + 1) * KS);
+      cp_async_wait1();
+    } else {
+      cp_async_wait0();
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < KS; kk += 16) {
+      uint32_t a[4];
+      {  // A: 16 tokens x 16 k of this warp (row-major)
+        const int r = warp * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
+        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[buf][r][c])), a[0], a[1], a[2], a[3]);
+      }
+#pragma unroll
+      for (int j = 0; j < TE / 8; ++j) {
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {  // B: 8 experts x 16 k (expert rows, k contiguous)
+          const int r = j * 8 + (lane & 7), c = kk + ((lane >> 3) & 1) * 8;
+          uint32_t b0, b1;
+          ldmatrix_x2(static_cast<uint32_t>(__cvta_generic_to_shared(&ws[buf][part][r][c])), b0, b1);
+          mma_bf16_16816(acc[j], a, b0, b1);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // C fragment: rows g, g+8 (tokens), columns 2t, 2t+1 (experts)
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < TE / 8; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tok = t0 + warp * 16 + g + 8 * (c >> 1), e = e0 + j * 8 + 2 * t + (c & 1);
+      if (tok < n_tok && e < n_exp) logits[(size_t)tok * n_exp + e] = acc[j][c] + (b ? b[e] : 0.f);
+    }
+}
+
+// w -> (hi, mid, lo) bf16 parts with w = hi + mid + lo (round to nearest at each step).
+__global__ void split3_kernel(const float* __restrict__ w, size_t n, __nv_bfloat16* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = lo;
+  }
+}
+
+}  // namespace
+
+void launch_router_split(const float* w, size_t n, __nv_bfloat16* w3, cudaStream_t s) {
+  split3_kernel<<<152 * 4, 256, 0, s>>>(w, n, w3);
+}
+
+void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
+                      float* logits, cudaStream_t s) {
+  dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
+  router_tc_kernel<<<grid, 128, 0, s>>>(x, n_tok, d, w3, b, n_exp, logits);
+}
+
+}  // namespace ds4
