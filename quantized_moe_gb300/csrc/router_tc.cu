@@ -2,9 +2,9 @@
 //
 // The fp32 router weights are split once, at create time, into three bf16 parts
 // w = w_hi + w_mid + w_lo (8 + 8 + 8 significand bits cover all 24 of fp32). The activations are
-// bf16 already, so every product x * w_part is exact in fp32, and an m16n8k16 bf16 MMA with an
-// fp32 accumulator over the three parts gives the fp32 dot product: the same accuracy as fp32
-// FMAs on the CUDA cores, at tensor-core throughput.
+// bf16 already, so every product x * w_part is exact in fp32; the three MMAs of each 16-wide K
+// step go into a fresh fp32 accumulator, which is added to the running sum with ordinary fp32
+// adds: the accuracy of fp32 FMAs on the CUDA cores, at tensor-core throughput.
 //
 // CTA = 64 tokens x 64 experts, 4 warps (16 tokens each, all 64 experts); K staged through
 // shared memory 32 at a time, double-buffered with cp.async.
@@ -89,13 +89,19 @@ __global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __r
       }
 #pragma unroll
       for (int j = 0; j < TE / 8; ++j) {
+        // The tensor core's accumulation truncates; a long chain of MMAs into one accumulator
+        // would bias the sum. Each 16-wide K step therefore starts from zero and is added to
+        // the running fp32 sum with round-to-nearest adds.
+        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int part = 0; part < 3; ++part) {  // B: 8 experts x 16 k (expert rows, k contiguous)
           const int r = j * 8 + (lane & 7), c = kk + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1;
           ldmatrix_x2(static_cast<uint32_t>(__cvta_generic_to_shared(&ws[buf][part][r][c])), b0, b1);
-          mma_bf16_16816(acc[j], a, b0, b1);
+          mma_bf16_16816(tmp, a, b0, b1);
         }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][c] += tmp[c];
       }
     }
     __syncthreads();
