@@ -212,6 +212,29 @@ def run_reference(args, spec, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks (host logic)
+
+def batch_seed(spec: synthetic.Spec, rank: int, batch: int, batches: int) -> int:
+    """Seed of input batch `batch` on `rank`: every rank draws its own tokens (replicas share weights)."""
+    return spec.seed + 7919 * (rank * batches + batch + 1)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's value (timings are reduced with MAX; world 1 returns the value)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_step: int, steps: int, seconds: float) -> float:
+    """Tokens per second of all ranks together: every rank runs `steps` steps of its own tokens."""
+    return world * tokens_per_step * steps / seconds
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def main():
@@ -271,7 +294,7 @@ def main():
     # per-rank input batches (different tokens per step, and per rank)
     xs, tids = [], []
     for b in range(args.batches):
-        sb = spec.with_(seed=spec.seed + 7919 * (rank * args.batches + b + 1))
+        sb = spec.with_(seed=batch_seed(spec, rank, b, args.batches))
         xs.append(torch.from_numpy(synthetic.activations(sb).view(np.int16)).to(dev))
         if spec.n_hash:
             r = np.random.default_rng(sb.seed)
@@ -321,13 +344,8 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = world * spec.n_tokens * args.steps
-    value = tokens / (total_ms / 1e3)
+    total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
+    value = whole_job_rate(world, spec.n_tokens, args.steps, total_ms / 1e3)
     ms_per_step = total_ms / args.steps
 
     # per-launch times of the same workload: events recorded between the launches (this
@@ -358,12 +376,8 @@ def main():
                                 spec.n_hash, out_host.data_ptr(), stream.cuda_stream)
         if i >= args.warmup:
             e2e_s.append(time.perf_counter() - t0)
-    e2e_total = float(sum(e2e_s))
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = tokens / e2e_total
+    e2e_total = max_over_ranks(float(sum(e2e_s)), world, dev)
+    e2e_value = whole_job_rate(world, spec.n_tokens, args.steps, e2e_total)
 
     launches = api.ds4moe_launches_per_forward(h, spec.n_tokens) * args.steps
     api.ds4moe_destroy(h)
