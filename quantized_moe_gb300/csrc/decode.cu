@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
       const bool ok = id >= 0 && id < a.vocab;
       if (!ok && lane == 0) atomicOr(a.err, 1);
       if (lane < K) {
-        const int ex = ok ? a.table[(size_t)id * K + lane] : 0;
+        const int ex = ok ? a.table[(size_t)id * K + lane] : lane;  // bad id: distinct experts, weight 0
         a.idx[t * K + lane] = ex;
         a.wts[t * K + lane] = ok ? 1.f / (float)K : 0.f;
         s_idx[t * K + lane] = ex;

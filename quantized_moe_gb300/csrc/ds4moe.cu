@@ -318,12 +318,17 @@ int repack_stack(ds4moe_handle* h, int fmt, const void* src, uint8_t* dst, int n
 }
 
 // Every table entry must name a routed expert: the bucketing indexes per-expert arrays by it.
-int check_table(const int* dev_table, size_t n, int n_exp) {
-  std::vector<int> host(n);
-  DS4_CUDA(cudaMemcpy(host.data(), dev_table, n * 4, cudaMemcpyDeviceToHost));
-  for (size_t i = 0; i < n; ++i)
+int check_table(const int* dev_table, size_t rows, int k, int n_exp) {
+  std::vector<int> host(rows * k);
+  DS4_CUDA(cudaMemcpy(host.data(), dev_table, host.size() * 4, cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < host.size(); ++i)
     if (host[i] < 0 || host[i] >= n_exp)
       return fail(DS4MOE_ERR_INVALID_ARG, "hash_table entry %zu is %d, outside [0, n_experts=%d)", i, host[i], n_exp);
+  for (size_t r = 0; r < rows; ++r)  // a token is routed to k distinct experts
+    for (int a = 0; a < k; ++a)
+      for (int b = a + 1; b < k; ++b)
+        if (host[r * k + a] == host[r * k + b])
+          return fail(DS4MOE_ERR_INVALID_ARG, "hash_table row %zu names expert %d twice", r, host[r * k + a]);
   return DS4MOE_OK;
 }
 
@@ -423,7 +428,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   if (s->hash_vocab > 0) {
     DS4_TRY(h->alloc_t(&h->table, (size_t)s->hash_vocab * K * 4));
     DS4_TRY(copy_in(h->table, w->hash_table, (size_t)s->hash_vocab * K * 4, s->device, "hash_table"));
-    DS4_TRY(check_table(h->table, (size_t)s->hash_vocab * K, E));
+    DS4_TRY(check_table(h->table, (size_t)s->hash_vocab, K, E));
   }
   // workspace for max_tokens
   const size_t M = (size_t)s->max_tokens, slots = M * K;
@@ -479,6 +484,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counter, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->hmax, 0, (slots + M) * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     rc = fail(DS4MOE_ERR_CUDA, "workspace init: %s", cudaGetErrorString(e));

@@ -34,15 +34,17 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase of the given parity. Returns false (and raises the CTA's abort flag and
-// error bit 2 of *err) if it does not complete in time, or if another thread already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err) {
+// Waits for the phase of the given parity. Returns false (and raises the CTA's abort flag, error
+// bit 2 of *err and bit 16 + site, which names the wait that gave up) if it does not complete in
+// time, or if another thread already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int site = 0) {
   const long long t0 = clock64();
   while (!mbar_try(b, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > kTimeoutCycles) {
       *abort_flag = 1;
-      atomicOr(err, 4);
+      atomicOr(err, 4 | (1 << (16 + site)));
       return false;
     }
   }
