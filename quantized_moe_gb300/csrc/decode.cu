@@ -465,11 +465,52 @@ __device__ __forceinline__ DownItem down_item(const DecodeArgs& a, int i, int n_
   return it;
 }
 
-// One item: the unit times the item's h rows (in passes of 4), added to the warp's partial rows.
+// The lane's h values (two float2 per chunk) and max|h| of the first pass of an item's rows,
+// loaded together with its weight unit so that the first pass waits on no L2 round trip.
+template <int P>
+struct HPre {
+  float2 v[P][2][2];
+  float hm[P];
+};
+
+template <int FMT, int P>
+__device__ __forceinline__ void h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* hbase = it.shared ? a.Hs : a.H;
+  const float* hmax = it.shared ? a.hmax + a.n_tok * a.top_k : a.hmax;
+  const int kdim = it.shared ? a.fs : a.f;
+#pragma unroll
+  for (int tt = 0; tt < P; ++tt) {
+    if (tt >= it.cnt) break;
+    const int row = it.pos0 + tt;
+    hp.hm[tt] = __ldcg(hmax + row);
+#pragma unroll
+    for (int c = 0; c < Unit<FMT>::kChunks; ++c) {
+      const float* base = hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c;
+      hp.v[tt][c][0] = __ldcg(reinterpret_cast<const float2*>(base + 16 * g + 2 * t));
+      hp.v[tt][c][1] = __ldcg(reinterpret_cast<const float2*>(base + 16 * g + 2 * t + 8));
+    }
+  }
+}
+
+// B fragment from h values already in registers (what xfrag_f32 computes after its loads).
+__device__ __forceinline__ XFrag xfrag_vals(float2 v0, float2 v1, float sc) {
+  const __half2 h0 = __floats2half2_rn(v0.x * sc, v0.y * sc);
+  const __half2 h1 = __floats2half2_rn(v1.x * sc, v1.y * sc);
+  XFrag f;
+  f.b0 = h2_bits(h0);
+  f.b1 = h2_bits(h1);
+  const float2 a = __half22float2(h0), b = __half22float2(h1);
+  xfrag_sums(f, (a.x + a.y) + (b.x + b.y));
+  return f;
+}
+
+// One item: the unit times the item's h rows (in passes of P), added to the warp's partial rows.
+// The first pass uses the prefetched values.
 template <int FMT, int P>
 __device__ __forceinline__ void down_item_compute(const DecodeArgs& a, const DownItem& it, const Unit<FMT>& u,
-                                                  float* part_rows, const BMask& bm, const Q2kLaneConst& qc,
-                                                  int kdim) {
+                                                  const HPre<P>& hp, float* part_rows, const BMask& bm,
+                                                  const Q2kLaneConst& qc, int kdim) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* hbase = it.shared ? a.Hs : a.H;
   const float* hmax = it.shared ? a.hmax + a.n_tok * a.top_k : a.hmax;
@@ -481,10 +522,16 @@ __device__ __forceinline__ void down_item_compute(const DecodeArgs& a, const Dow
     for (int tt = 0; tt < P; ++tt) {
       if (tt >= np) break;
       const int row = it.pos0 + p0 + tt;
-      sc[tt] = fp16_row_scale(__ldcg(hmax + row));
+      if (p0 == 0) {
+        sc[tt] = fp16_row_scale(hp.hm[tt]);
 #pragma unroll
-      for (int c = 0; c < Unit<FMT>::kChunks; ++c)
-        xf[tt][c] = xfrag_f32(hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c, sc[tt]);
+        for (int c = 0; c < Unit<FMT>::kChunks; ++c) xf[tt][c] = xfrag_vals(hp.v[tt][c][0], hp.v[tt][c][1], sc[tt]);
+      } else {
+        sc[tt] = fp16_row_scale(__ldcg(hmax + row));
+#pragma unroll
+        for (int c = 0; c < Unit<FMT>::kChunks; ++c)
+          xf[tt][c] = xfrag_f32(hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c, sc[tt]);
+      }
     }
     float acc[P][2];
 #pragma unroll
@@ -563,12 +610,21 @@ __device__ __forceinline__ void down_load(const DownItem& it, RawUnit& b, int rg
 }
 
 template <int FMT_R, int FMT_S, int P>
-__device__ __forceinline__ void down_item_run(const DecodeArgs& a, const DownItem& it, const RawUnit& b, float* part,
-                                              float* parts, const BMask& bm, const Q2kLaneConst& qc) {
+__device__ __forceinline__ void down_item_run(const DecodeArgs& a, const DownItem& it, const RawUnit& b,
+                                              const HPre<P>& hp, float* part, float* parts, const BMask& bm,
+                                              const Q2kLaneConst& qc) {
   if (it.shared)
-    down_item_compute<FMT_S, P>(a, it, as_unit<FMT_S>(b), parts, bm, qc, a.fs);
+    down_item_compute<FMT_S, P>(a, it, as_unit<FMT_S>(b), hp, parts, bm, qc, a.fs);
   else
-    down_item_compute<FMT_R, P>(a, it, as_unit<FMT_R>(b), part, bm, qc, a.f);
+    down_item_compute<FMT_R, P>(a, it, as_unit<FMT_R>(b), hp, part, bm, qc, a.f);
+}
+
+template <int FMT_R, int FMT_S, int P>
+__device__ __forceinline__ void down_h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp) {
+  if (it.shared)
+    h_prefetch<FMT_S, P>(a, it, hp);
+  else
+    h_prefetch<FMT_R, P>(a, it, hp);
 }
 
 template <int FMT_R, int FMT_S, int P>
@@ -599,17 +655,23 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int
     down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
   }
   pdl_wait();
+  // h of the two preloaded items (H is complete now); later items fetch theirs with their units
+  HPre<P> h0, h1;
+  if (warp < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0);
+  if (warp + kWarps < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1);
   for (int i = warp; i < n_items; i += 2 * kWarps) {
-    down_item_run<FMT_R, FMT_S, P>(a, it0, b0, part, parts, bm, qc);
+    down_item_run<FMT_R, FMT_S, P>(a, it0, b0, h0, part, parts, bm, qc);
     if (i + 2 * kWarps < n_items) {
       it0 = down_item(a, i + 2 * kWarps, n_routed, n_kb_r);
       down_load<FMT_R, FMT_S>(it0, b0, rg, n_kb_r, n_kb_s);
+      down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0);
     }
     if (i + kWarps < n_items) {
-      down_item_run<FMT_R, FMT_S, P>(a, it1, b1, part, parts, bm, qc);
+      down_item_run<FMT_R, FMT_S, P>(a, it1, b1, h1, part, parts, bm, qc);
       if (i + 3 * kWarps < n_items) {
         it1 = down_item(a, i + 3 * kWarps, n_routed, n_kb_r);
         down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
+        down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1);
       }
     }
   }
