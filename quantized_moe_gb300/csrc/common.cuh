@@ -186,6 +186,7 @@ struct GemmArgs {
   const int4* tiles;       // routed: device tile list (expert, first row, rows); nullptr: dense
   const int* n_tiles;      // routed: number of tiles
   int n_rows;              // dense: rows of the activation operand (tokens)
+  int m_tiles;             // 128-row slices of the weight matrix (set by launch_gemm)
   const float* inv_scale;  // gate/up: 1 / fp16 scale of each activation row
   __half* h_out;           // gate/up output [row][ld_out] fp16
   float* y_out;            // down output [row][ld_out] fp32

@@ -1,21 +1,30 @@
 // Prefill expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
-// One CTA computes a 128-row x N-token tile (N <= 256, a multiple of 64) of one expert:
+// Persistent: one CTA per SM loops over work items, each a 128-row x N-token tile (N <= 256, a
+// multiple of 64) of one expert:
 //   gate/up: the 128 rows interleave 64 gate rows and the 64 up rows of the same features, so
 //            the epilogue forms h = silu(g) * u for 64 features and writes it as fp16;
 //   down:    128 rows of d, written as fp32 per bucketed slot for the fixed-order combine.
-// Warp roles (10 warps):
-//   warp 0     producer: bulk-copies the packed weight units of each K unit (256 k for Q2_K,
-//              128 k for Q8_0) and TMA-loads the activation tile (fp16, 128-byte swizzle) of
-//              each 64-wide K stage;
+// The weight, activation and dequantized-tile pipelines run on across items, and the fp32
+// accumulator is double-buffered in TMEM (2 x 256 columns), so the epilogue of one item overlaps
+// the main loop of the next.
+// Warp roles (19 warps):
+//   warp 0     weight producer: bulk-copies the packed weight units of each K unit (256 k for
+//              Q2_K, 128 k for Q8_0) of the tile's rows;
 //   warp 1     allocates TMEM; one thread issues the tcgen05.mma of every stage;
-//   warps 2-9  dequantize: each turns one 16-row packed unit into fp16 weights in registers
-//              (exact small-integer quants, fp16 FMA with the sub-block scale and min) and
-//              writes them with stmatrix straight into the swizzled A tile; afterwards they run
-//              the epilogue from TMEM (tcgen05.ld).
+//   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
+//              64-wide K stage;
+//   warps 3-18 dequantize: two warps per 16-row group, each turning half of the group's 64-wide
+//              K stage into fp16 weights in registers (exact small-integer quants, one fp16 FMA
+//              with the sub-block scale and min) and writing them with stmatrix straight into the
+//              swizzled A tile;
+//   warps 19-22 epilogue: read the accumulator from TMEM (tcgen05.ld), one warp per lane
+//              quadrant, and release its buffer to the MMA.
 // Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
 // unwinds instead of hanging.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "tc_ptx.cuh"
 
@@ -25,14 +34,17 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_STAGES = 2;  // dequantized weight tiles (written on chip: little latency to hide)
-constexpr int B_STAGES = 4;  // activation tiles (TMA from L2/HBM)
+constexpr int A_STAGES = 3;  // dequantized weight tiles
+constexpr int B_STAGES = 3;  // activation tiles (TMA from L2/HBM)
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
-constexpr int kDeqWarps = 8;
-constexpr int kThreads = (2 + kDeqWarps) * 32;  // 320
-constexpr int TMEM_COLS = 256;
+constexpr int kDeqWarps = 16;
+constexpr int kFirstDeq = 3;  // warps 0-2: weight producer, MMA, activation producer
+constexpr int kEpiWarps = 4;  // warps 19-22: epilogue, one per TMEM lane quadrant
+constexpr int kThreads = (kFirstDeq + kDeqWarps + kEpiWarps) * 32;  // 736
+constexpr int ACC_COLS = 256;            // one fp32 accumulator of 128 x BN
+constexpr int TMEM_COLS = 2 * ACC_COLS;  // double-buffered: the epilogue of one item overlaps the next
 
 // Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
 // Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
@@ -44,10 +56,10 @@ struct Cfg {
   static constexpr int OFF_B = OFF_A + A_STAGES * A_BYTES;
   static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
-  static constexpr int N_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * RAWS + 1;
+  static constexpr int N_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
-  static constexpr int GBUF_BYTES = 2 * 64 * 16 * 4;  // per epilogue group: 16 columns x 64 gate rows fp32
+  static constexpr int GBUF_BYTES = 64 * 16 * 4;  // 16 columns x 64 gate rows fp32 (epilogue exchange)
   static constexpr int SMEM_BYTES = OFF_GBUF + GBUF_BYTES + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -59,7 +71,8 @@ struct Bars {
   uint64_t* b_empty;    // [B_STAGES] MMA commit -> producer
   uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
   uint64_t* raw_empty;  // [RAWS] dequant -> producer
-  uint64_t* acc_full;   // MMA -> epilogue
+  uint64_t* acc_full;   // [2] MMA -> epilogue
+  uint64_t* acc_empty;  // [2] epilogue -> MMA
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -74,62 +87,103 @@ __device__ __forceinline__ uint32_t a_row_addr(uint32_t a_base, int rg16, int sb
   return a_base + (row >> 3) * 1024 + (row & 7) * 128 + ((kc ^ (row & 7)) << 4);
 }
 
-// Dequantize the 16 rows x 64 k of one Q2_K unit that fall in K stage su (0..3) and store them.
-__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int rg16) {
+// Dequantize half (32 k: two 16-k sub-blocks) of the 16 rows x 64 k of one Q2_K unit that fall in
+// K stage su (0..3) and store them.
+__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int rg16, int half) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
-  const int c = su >> 1, i0 = (su & 1) * 4;
+  const int c = su >> 1, i0 = (su & 1) * 4 + 2 * half;  // first sub-block of the chunk handled here
   const uint4 qw = lds128(unit + c * 512 + 16 * lane);
   const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
-  const uint32_t sca = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
-  const uint32_t scb = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  // scale bytes of sub-blocks i0, i0 + 1: byte 0/1 row g, byte 2/3 row g + 8
+  const uint32_t scw = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
   const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
   // (d of row g, d of row g+8) times 2^16: exact (only the exponent changes); create refuses
   // super-blocks whose d * 15 * 2^16 would leave the fp16 range
   const __half2 k256 = __float2half2_rn(256.f);
   const __half2 d2 = __hmul2(__hmul2(u2h(prmt(dd0, dd1, 0x5410u)), k256), k256);
-  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));   // (dmin of row g, dmin of row g+8)
+  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));  // (dmin of row g, dmin of row g+8)
+  // m is read as the fp16 1024 + m; one FMA with -dmin and 1024 dmin (exact: a power of two)
+  // then gives -dmin * m rounded once
+  const __half2 ndm2 = __hneg2(dm2);
   const __half2 k1024 = __float2half2_rn(1024.f);
+  const __half2 dm1024 = __hmul2(dm2, k1024);
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = i0 + ii;
-    const uint32_t sc = (ii < 2 ? sca : scb) >> (8 * (ii & 1));
-    // (s_g, s_g8) and (m_g, m_g8) as exact fp16 integers through the 1024 + x encoding
-    const __half2 s2 = __hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024);
-    const __half2 m2 = __hsub2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), k1024);
-    const __half2 ds = __hmul2(s2, d2);             // 2^16 * d*s of rows g, g+8, rounded once to fp16
-    const __half2 ndm = __hneg2(__hmul2(m2, dm2));  // -(dmin*m)
-    const __half2 ds_g = u2h(prmt(h2u(ds), 0u, 0x1010u)), ds_h = u2h(prmt(h2u(ds), 0u, 0x3232u));
-    const __half2 nm_g = u2h(prmt(h2u(ndm), 0u, 0x1010u)), nm_h = u2h(prmt(h2u(ndm), 0u, 0x3232u));
+  for (int j = 0; j < 2; ++j) {
+    const int i = i0 + j;
+    const uint32_t sc = scw >> (8 * j);
+    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), d2);  // 2^16 d s, rounded once
+    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), ndm2, dm1024);  // -dmin m
     uint32_t a[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       // the quant pair moved to mantissa bits 8-9: the exact fp16 subnormal q * 2^-16, so one
       // FMA with 2^16 d s gives d s q - dmin m with a single rounding
       const uint32_t qb = (i < 4 ? (w[r] << (8 - 2 * i)) : (w[r] >> (2 * i - 8))) & 0x03000300u;
-      a[r] = h2u(__hfma2(u2h(qb), (r & 1) ? ds_h : ds_g, (r & 1) ? nm_h : nm_g));
+      a[r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
+                         : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
     }
-    stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
+    stmatrix_x4(a_row_addr(a_base, rg16, 2 * half + j), a[0], a[1], a[2], a[3]);
   }
 }
 
-// Dequantize the 16 rows x 64 k of one Q8_0 unit (128 k) that fall in K stage su (0..1).
-__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int rg16) {
+// Dequantize half (two 16-k sub-blocks) of the 16 rows x 64 k of one Q8_0 unit (128 k) that fall
+// in K stage su (0..1).
+__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int rg16, int half) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const __half2 k1152 = __float2half2_rn(1152.f);
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = 4 * su + ii;  // MMA index (16-k sub-block) inside the unit
+  for (int j = 0; j < 2; ++j) {
+    const int ii = 2 * half + j;  // sub-block of the stage
+    const int i = 4 * su + ii;    // MMA index (16-k sub-block) inside the unit
     const uint4 v = lds128(unit + 512 * (i >> 1) + 16 * lane);
     const uint32_t wa = (i & 1) ? v.z : v.x, wb = (i & 1) ? v.w : v.y;
-    const uint32_t scw = lds32(unit + kQ80ScOff + 4 * (4 * g + (i >> 1)));  // block i/2, rows g, g+8
-    const __half2 s_g = u2h(prmt(scw, 0u, 0x1010u)), s_h = u2h(prmt(scw, 0u, 0x3232u));
+    const __half2 sc = u2h(lds32(unit + kQ80ScOff + 4 * (4 * g + (i >> 1))));  // block i/2: (row g, row g+8)
     const uint32_t raw[4] = {prmt(wa, 0x64u, 0x4140u), prmt(wa, 0x64u, 0x4342u), prmt(wb, 0x64u, 0x4140u),
                              prmt(wb, 0x64u, 0x4342u)};  // fp16 1024 + u, u = q + 128
     uint32_t a[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) a[r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? s_h : s_g));
+    for (int r = 0; r < 4; ++r)
+      a[r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? __high2half2(sc) : __low2half2(sc)));
     stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
   }
+}
+
+// Waits (bounded, without raising errors) for a phase: used only to let copies land before exit.
+__device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity) && clock64() - t0 < kTimeoutCycles) {
+  }
+}
+
+// The tile of work item `it` (token tile, 128-row slice of the weights).
+struct Item {
+  int expert, row0, rows, nbox, n, mt;
+};
+
+__device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
+  Item t;
+  const int tile = it / p.m_tiles;
+  t.mt = it - tile * p.m_tiles;
+  if (p.tiles) {
+    const int4 v = __ldg(p.tiles + tile);
+    t.expert = v.x;
+    t.row0 = v.y;
+    t.rows = v.z;
+  } else {
+    t.expert = -1;
+    t.row0 = tile * BN;
+    t.rows = min(BN, p.n_rows - t.row0);
+  }
+  t.nbox = (max(t.rows, 1) + BOX_ROWS - 1) / BOX_ROWS;
+  t.n = t.nbox * BOX_ROWS;
+  return t;
+}
+
+// Work items of the launch: (token tiles) x (128-row slices of the weights), slices fastest so that
+// the CTAs running at the same time share their activation tiles through L2.
+__device__ __forceinline__ int item_count(const GemmArgs& p) {
+  const int tiles = p.tiles ? *p.n_tiles : (p.n_rows + BN - 1) / BN;
+  return tiles * p.m_tiles;
 }
 
 template <int FMT, bool GATEUP>
@@ -139,29 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // ---- tile
-  int expert, row0, rows;
-  if (p.tiles) {
-    if ((int)blockIdx.y >= *p.n_tiles) return;
-    const int4 t = p.tiles[blockIdx.y];
-    expert = t.x; row0 = t.y; rows = t.z;
-  } else {
-    expert = -1;
-    row0 = blockIdx.y * BN;
-    rows = min(BN, p.n_rows - row0);
-  }
-  if (rows <= 0) return;
-  const int nbox = (rows + BOX_ROWS - 1) / BOX_ROWS;
-  const int n = nbox * BOX_ROWS;  // MMA N
-  const int mt = blockIdx.x;
   constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
   const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
-  const size_t eoff = expert >= 0 ? (size_t)expert * p.mat_bytes : 0;
-  const uint8_t* src0 = p.w0 + eoff;
-  const uint8_t* src1 = GATEUP ? p.w1 + eoff : nullptr;
+  const int n_items = item_count(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
   const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
-  const int rg0 = GATEUP ? 4 * mt : 8 * mt;  // first 16-row group of the tile's rows
 
   Bars b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -171,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   b.b_empty = bars + 2 * A_STAGES + B_STAGES;
   b.raw_full = bars + 2 * A_STAGES + 2 * B_STAGES;
   b.raw_empty = b.raw_full + RAWS;
-  b.acc_full = b.raw_empty + RAWS;
+  b.acc_full = b.raw_empty + RAWS;   // [2]
+  b.acc_empty = b.acc_full + 2;      // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* gbuf = reinterpret_cast<float*>(smem + C::OFF_GBUF);
@@ -189,7 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       mbar_init(&b.raw_full[r], 1);
       mbar_init(&b.raw_empty[r], kDeqWarps);
     }
-    mbar_init(b.acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.acc_full[i], 1);
+      mbar_init(&b.acc_empty[i], kEpiWarps);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -203,125 +243,160 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ weight producer
     if (lane == 0) {
-      // Two independent streams, each issued as soon as its buffer is free: the weight units (up
-      // to RAWS K units ahead of the dequant warps) and the activation tiles (up to B_STAGES
-      // stages ahead of the MMA). Neither waits for the other.
-      int sB = 0, uN = 0;
-      long long last = clock64();
-      while ((sB < n_stages || uN < n_kb) && !*abort_flag) {
-        bool progressed = false;
-        if (uN < n_kb && mbar_try(&b.raw_empty[uN % RAWS], ((uN / RAWS) & 1) ^ 1)) {
-          const int rs = uN % RAWS;
+      uint32_t gu = 0;  // K units issued by this CTA over all its items
+      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
+        const Item t = item_of(p, it);
+        const size_t eoff = t.expert >= 0 ? (size_t)t.expert * p.mat_bytes : 0;
+        const uint8_t* src0 = p.w0 + eoff;
+        const uint8_t* src1 = GATEUP ? p.w1 + eoff : nullptr;
+        const int rg0 = GATEUP ? 4 * t.mt : 8 * t.mt;  // first 16-row group of the slice
+        for (int uN = 0; uN < n_kb; ++uN, ++gu) {
+          const int rs = gu % RAWS;
+          if (!mbar_wait(&b.raw_empty[rs], ((gu / RAWS) & 1) ^ 1, abort_flag, p.err, 1)) break;
           unsigned char* dst = smem + C::OFF_RAW + rs * C::RAW_BYTES;
           mbar_expect_tx(&b.raw_full[rs], GATEUP ? 2 * raw_copy : raw_copy);
           bulk_load(dst, src0 + unit_offset(rg0, uN, n_kb, UB), raw_copy, &b.raw_full[rs]);
           if (GATEUP) bulk_load(dst + raw_copy, src1 + unit_offset(rg0, uN, n_kb, UB), raw_copy, &b.raw_full[rs]);
-          ++uN;
-          progressed = true;
-        }
-        if (sB < n_stages && mbar_try(&b.b_empty[sB % B_STAGES], ((sB / B_STAGES) & 1) ^ 1)) {
-          const int sb = sB % B_STAGES;
-          unsigned char* bdst = smem + C::OFF_B + sb * B_BYTES;
-          mbar_expect_tx(&b.b_full[sb], nbox * BOX_ROWS * BK * 2);
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, row0 + bx * BOX_ROWS, &b.b_full[sb]);
-          ++sB;
-          progressed = true;
-        }
-        if (progressed) {
-          last = clock64();
-        } else if (clock64() - last > kTimeoutCycles) {
-          *abort_flag = 1;
-          atomicOr(p.err, 4);
         }
       }
+      // the last copies land before the CTA may exit (after an abort they may still be in flight)
+      for (uint32_t k = gu > (uint32_t)RAWS ? gu - RAWS : 0; k < gu; ++k) bounded_try(&b.raw_full[k % RAWS], (k / RAWS) & 1);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ activation producer
+    if (lane == 0) {
+      uint32_t gs = 0;  // stages issued over all items
+      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
+        const Item t = item_of(p, it);
+        for (int sB = 0; sB < n_stages; ++sB, ++gs) {
+          const int sb = gs % B_STAGES;
+          if (!mbar_wait(&b.b_empty[sb], ((gs / B_STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
+          unsigned char* bdst = smem + C::OFF_B + sb * B_BYTES;
+          mbar_expect_tx(&b.b_full[sb], t.nbox * BOX_ROWS * BK * 2);
+          for (int bx = 0; bx < t.nbox; ++bx)
+            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, t.row0 + bx * BOX_ROWS, &b.b_full[sb]);
+        }
+      }
+      for (uint32_t k = gs > (uint32_t)B_STAGES ? gs - B_STAGES : 0; k < gs; ++k)
+        bounded_try(&b.b_full[k % B_STAGES], (k / B_STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BM, n);
-      for (int s = 0; s < n_stages; ++s) {
-        const int sa = s % A_STAGES, sb = s % B_STAGES;
-        if (!mbar_wait(&b.a_full[sa], (s / A_STAGES) & 1, abort_flag, p.err)) break;
-        if (!mbar_wait(&b.b_full[sb], (s / B_STAGES) & 1, abort_flag, p.err)) break;
+      uint32_t gs = 0;
+      int local = 0;  // items of this CTA so far: accumulator buffer local & 1
+      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++local) {
+        const Item t = item_of(p, it);
+        const int buf = local & 1;
+        // the epilogue has drained this buffer (item local - 2)
+        if (!mbar_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6)) break;
         tc_fence_after();
-        const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + sa * A_BYTES));
-        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + sb * B_BYTES));
+        const uint32_t idesc = idesc_f16_f32(BM, t.n);
+        const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS);
+        bool ok = true;
+        for (int s = 0; s < n_stages; ++s, ++gs) {
+          const int sa = gs % A_STAGES, sb = gs % B_STAGES;
+          if (!mbar_wait(&b.a_full[sa], (gs / A_STAGES) & 1, abort_flag, p.err, 7) ||
+              !mbar_wait(&b.b_full[sb], (gs / B_STAGES) & 1, abort_flag, p.err, 8)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + sa * A_BYTES));
+          const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + sb * B_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
-          tc_mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-        tc_commit(&b.a_empty[sa]);
-        tc_commit(&b.b_empty[sb]);
+          for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
+            tc_mma_f16(acc, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+          tc_commit(&b.a_empty[sa]);
+          tc_commit(&b.b_empty[sb]);
+        }
+        if (!ok) break;
+        tc_commit(&b.acc_full[buf]);
       }
-      tc_commit(b.acc_full);
+    }
+  } else if (warp < kFirstDeq + kDeqWarps) {
+    // ------------------------------------------------------------------ dequant
+    const int dw = warp - kFirstDeq;
+    const int rgw = dw & 7, half = dw >> 3;  // 16-row group of the slice, half of each K stage
+    uint32_t gs = 0;
+    for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
+      bool ok = true;
+      for (int s = 0; s < n_stages; ++s, ++gs) {
+        // the raw units follow the stages: unit gs / kpu of the CTA's sequence
+        const uint32_t gu = gs / kpu;
+        const int rs = gu % RAWS, sa = gs % A_STAGES, su = gs % kpu;
+        if (su == 0 && !mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
+        if (!mbar_wait(&b.a_empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
+        const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
+        const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
+        if (FMT == FMT_Q2_K)
+          deq_q2k(unit, su, a_base, rgw, half);
+        else
+          deq_q80(unit, su, a_base, rgw, half);
+        fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&b.a_full[sa]);
+          if (su == kpu - 1) mbar_arrive(&b.raw_empty[rs]);
+        }
+      }
+      if (!ok) break;
     }
   } else {
-    // ------------------------------------------------------------------ dequant
-    const int dw = warp - 2;  // 16-row group of the tile this warp writes
-    for (int s = 0; s < n_stages; ++s) {
-      const int u = s / kpu, rs = u % RAWS, sa = s % A_STAGES, su = s % kpu;
-      if (su == 0 && !mbar_wait(&b.raw_full[rs], (u / RAWS) & 1, abort_flag, p.err)) break;
-      if (!mbar_wait(&b.a_empty[sa], ((s / A_STAGES) & 1) ^ 1, abort_flag, p.err)) break;
-      const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + dw * UB);
-      const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
-      if (FMT == FMT_Q2_K)
-        deq_q2k(unit, su, a_base, dw);
-      else
-        deq_q80(unit, su, a_base, dw);
-      fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&b.a_full[sa]);
-        if (su == kpu - 1) mbar_arrive(&b.raw_empty[rs]);
-      }
-    }
     // ------------------------------------------------------------------ epilogue
-    if (mbar_wait(b.acc_full, 0, abort_flag, p.err)) {
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+    const int row = 32 * quad + lane;     // slice row = TMEM lane
+    int local = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
+      const Item t = item_of(p, it);
+      const int buf = local & 1;
+      // all four warps enter the item's epilogue (it has named barriers) only together
+      if (!named_bar_all(1, 32 * kEpiWarps, mbar_wait(&b.acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 5)))
+        break;
       tc_fence_after();
-      const int grp = (warp - 2) >> 2;        // two groups of four warps split the columns
-      const int quad = warp & 3;              // TMEM lane quadrant this warp may access
-      const int row = 32 * quad + lane;       // tile row = TMEM lane
-      const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-      float* gb = gbuf + grp * 64 * 16;       // [column][gate row]: conflict-free by lane
-      for (int c0 = 16 * grp; c0 < n; c0 += 32) {
+      const uint32_t taddr = tmem + (uint32_t)(buf * ACC_COLS) + ((uint32_t)(32 * quad) << 16);
+      for (int c0 = 0; c0 < t.n; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(taddr + c0, r);
         tmem_ld_wait();
         if (GATEUP) {
           if (quad < 2) {  // gate rows: hand g to the up warps through shared memory
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gb[j * 64 + row] = __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j) gbuf[j * 64 + row] = __uint_as_float(r[j]);
           }
-          named_bar(1 + grp, 128);
+          named_bar(1, 32 * kEpiWarps);
           if (quad >= 2) {
-            const int feat = 64 * mt + row - 64;
+            const int feat = 64 * t.mt + row - 64;
             float inv[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) inv[j] = c0 + j < rows ? __ldg(p.inv_scale + row0 + c0 + j) : 0.f;
+            for (int j = 0; j < 16; ++j) inv[j] = c0 + j < t.rows ? __ldg(p.inv_scale + t.row0 + c0 + j) : 0.f;
             unsigned bad = 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
-              if (col < rows) {
-                const float h = silu_mul(gb[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
+              if (col < t.rows) {
+                const float h = silu_mul(gbuf[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
                 bad |= !(fabsf(h) <= 65504.f);
-                p.h_out[(size_t)(row0 + col) * p.ld_out + feat] = __float2half_rn(h);
+                p.h_out[(size_t)(t.row0 + col) * p.ld_out + feat] = __float2half_rn(h);
               }
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 8);
           }
-          named_bar(1 + grp, 128);
+          named_bar(1, 32 * kEpiWarps);
         } else {
-          const int drow = 128 * mt + row;
+          const int drow = 128 * t.mt + row;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < rows) p.y_out[(size_t)(row0 + col) * p.ld_out + drow] = __uint_as_float(r[j]);
+            if (col < t.rows) p.y_out[(size_t)(t.row0 + col) * p.ld_out + drow] = __uint_as_float(r[j]);
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.acc_empty[buf]);  // the MMA may overwrite this buffer
     }
   }
   tc_fence_before();
@@ -353,9 +428,18 @@ cudaError_t gemm_prepare() {
   return e;
 }
 
-cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& p, int m_tiles, int n_tiles,
+// Persistent launch: one CTA per SM (at most), each looping over the (token tile, weight slice)
+// items; n_tiles bounds the token tiles (the routed count itself is read on the device).
+cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& args, int m_tiles, int n_tiles,
                         cudaStream_t s) {
-  const dim3 grid(m_tiles, n_tiles);
+  static int n_sm[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !n_sm[dev]) cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = (dev >= 0 && dev < 64 && n_sm[dev] > 0) ? n_sm[dev] : 152;
+  GemmArgs p = args;
+  p.m_tiles = m_tiles;
+  const dim3 grid(std::max(1, std::min(sms, m_tiles * n_tiles)));
   if (fmt == FMT_Q2_K) return gateup ? launch_one<FMT_Q2_K, true>(tm, p, grid, s) : launch_one<FMT_Q2_K, false>(tm, p, grid, s);
   return gateup ? launch_one<FMT_Q8_0, true>(tm, p, grid, s) : launch_one<FMT_Q8_0, false>(tm, p, grid, s);
 }

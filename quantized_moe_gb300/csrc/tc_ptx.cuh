@@ -133,6 +133,17 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier that also returns the AND of a predicate over its threads: every participant
+// gets the same answer (so a group decides together whether to enter code with more barriers).
+__device__ __forceinline__ bool named_bar_all(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
