@@ -34,13 +34,26 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that may suspend the thread in hardware until the phase completes (or about 0.1 ms
+// pass): a waiting warp takes no issue slots from the warps that have work.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity), "r"(100000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of the given parity. Returns false (and raises the CTA's abort flag, error
 // bit 2 of *err and bit 16 + site, which names the wait that gave up) if it does not complete in
 // time, or if another thread already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
                                           int site = 0) {
+  if (mbar_try(b, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try(b, parity)) {
+  while (!mbar_try_sleep(b, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > kTimeoutCycles) {
       *abort_flag = 1;
