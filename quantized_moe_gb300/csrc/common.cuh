@@ -216,9 +216,10 @@ void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float*
                           float* logits, cudaStream_t s);
 void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const int* token_ids, int n_hash,
                  const int* table, int vocab, int* idx, float* wts, int* err, cudaStream_t s);
-void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* counts, cudaStream_t s);
-void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* counts, int* offsets, int* active,
-                           int* n_active, int* perm, int* rowof, cudaStream_t s);
+int bucket_chunks(int n_slots);  // ints of the bucketing scratch: bucket_chunks(n_slots) * n_exp
+void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* ghist, cudaStream_t s);
+void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, int* counts, int* offsets,
+                           int* active, int* n_active, int* perm, int* rowof, cudaStream_t s);
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s);
 

@@ -90,6 +90,7 @@ struct ds4moe_handle {
   int* n_active = nullptr;
   int* perm = nullptr;
   int* rowof = nullptr;
+  int* ghist = nullptr;  // batched bucketing: per-chunk expert histograms
   float* H = nullptr;   // decode: h per routed slot, fp32
   float* Hs = nullptr;  // decode: h of the shared expert, fp32
   float* Y = nullptr;   // prefill: down output per bucketed slot, fp32
@@ -441,6 +442,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->n_active, 4));
   DS4_TRY(h->alloc_t(&h->perm, slots * 4));
   DS4_TRY(h->alloc_t(&h->rowof, slots * 4));
+  DS4_TRY(h->alloc_t(&h->ghist, (size_t)ds4::bucket_chunks((int)slots) * E * 4));
   const size_t Md = std::min<size_t>(M, (size_t)ds4::decode_max_tokens());  // decode buffers
   DS4_TRY(h->alloc_t(&h->H, Md * K * f * 4));
   if (s->n_shared) DS4_TRY(h->alloc_t(&h->Hs, Md * fs * 4));
@@ -576,9 +578,10 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
   ds4::launch_topk(h->logits, n_learned, E, K, token_ids, n_hash, h->table, s.hash_vocab, h->idx, h->wts, h->err, st);
   mark("topk");
-  ds4::launch_bucket_count(h->idx, n * K, E, h->counts, st);
+  ds4::launch_bucket_count(h->idx, n * K, E, h->ghist, st);
   mark("bucket_count");
-  ds4::launch_bucket_scatter(h->idx, n * K, E, h->counts, h->offsets, h->active, h->n_active, h->perm, h->rowof, st);
+  ds4::launch_bucket_scatter(h->idx, n * K, E, h->ghist, h->counts, h->offsets, h->active, h->n_active, h->perm,
+                             h->rowof, st);
   mark("bucket_scatter");
   if (!h->has_prefill) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d needs the batched path, not sized at create", n);
   ds4::launch_xprep(xb, n, d, h->Xs16, h->inv_s, st);

@@ -65,7 +65,7 @@ __global__ void topk_kernel(const float* __restrict__ logits, int n_learned, int
     const bool ok = id >= 0 && id < vocab;
     if (!ok && lane == 0) atomicOr(err, 1);
     if (lane < top_k) {
-      idx[t * top_k + lane] = ok ? table[(size_t)id * top_k + lane] : 0;
+      idx[t * top_k + lane] = ok ? table[(size_t)id * top_k + lane] : lane;  // bad id: distinct experts, weight 0
       wts[t * top_k + lane] = ok ? 1.f / (float)top_k : 0.f;
     }
     return;
@@ -106,72 +106,93 @@ __global__ void topk_kernel(const float* __restrict__ logits, int n_learned, int
 }
 
 // CTA e counts the slots routed to expert e.
-__global__ void bucket_count_kernel(const int* __restrict__ idx, int n_slots, int* __restrict__ counts) {
-  __shared__ int part[32];
-  const int e = blockIdx.x;
-  int c = 0;
-  for (int i = threadIdx.x; i < n_slots; i += blockDim.x) c += idx[i] == e;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+// Bucketing in two passes over chunks of kChunk slots (one CTA each, 256 threads, E <= 256).
+constexpr int kChunk = 1024;
+
+// Pass 1: per-chunk histogram of the experts (integer counts, order-free).
+__global__ void __launch_bounds__(256) bucket_hist_kernel(const int* __restrict__ idx, int n_slots, int n_exp,
+                                                          int* __restrict__ ghist) {
+  __shared__ int hist[256];
+  if (threadIdx.x < n_exp) hist[threadIdx.x] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int tot = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += part[w];
-    counts[e] = tot;
-  }
+  const int s0 = blockIdx.x * kChunk;
+  for (int i = threadIdx.x; i < kChunk && s0 + i < n_slots; i += 256) atomicAdd(&hist[idx[s0 + i]], 1);
+  __syncthreads();
+  if (threadIdx.x < n_exp) ghist[(size_t)blockIdx.x * n_exp + threadIdx.x] = hist[threadIdx.x];
 }
 
-// CTA e: offset of expert e, its index among the active experts, and an order-preserving
-// compaction of its slots (so positions are sorted by (expert, token, slot)).
-__global__ void bucket_scatter_kernel(const int* __restrict__ idx, int n_slots, int n_exp,
-                                      const int* __restrict__ counts, int* __restrict__ offsets,
-                                      int* __restrict__ active, int* __restrict__ n_active, int* __restrict__ perm,
-                                      int* __restrict__ rowof) {
-  __shared__ int s_off, s_act, s_nact;
-  __shared__ int warp_tot[32];
-  const int e = blockIdx.x;
-  if (threadIdx.x == 0) { s_off = 0; s_act = 0; s_nact = 0; }
-  __syncthreads();
-  int off = 0, act = 0, nact = 0;
-  for (int i = threadIdx.x; i < n_exp; i += blockDim.x) {
-    const int c = counts[i];
-    if (i < e) { off += c; act += c > 0; }
-    nact += c > 0;
-  }
-  atomicAdd(&s_off, off);  // integer sums: order does not change the result
-  atomicAdd(&s_act, act);
-  atomicAdd(&s_nact, nact);
-  __syncthreads();
-  const int base = s_off;
-  if (threadIdx.x == 0) {
-    offsets[e] = base;
-    if (e == n_exp - 1) offsets[n_exp] = base + counts[e];
-    if (counts[e] > 0) active[s_act] = e;
-    if (e == 0) *n_active = s_nact;
-  }
-  if (counts[e] == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  int running = base;
-  for (int i0 = 0; i0 < n_slots; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    const bool hit = i < n_slots && idx[i] == e;
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    __syncthreads();
-    if (lane == 0) warp_tot[warp] = __popc(m);
-    __syncthreads();
-    int before = 0, tot = 0;
-    for (int w = 0; w < nw; ++w) {
-      const int c = warp_tot[w];
-      if (w < warp) before += c;
+// Pass 2: chunk b places its slots at offsets[e] + (slots of e in earlier chunks) + (earlier slots
+// of e in this chunk), so positions are sorted by (expert, slot) = (expert, token, slot). Ranks
+// inside a round of 256 slots come from warp match masks and per-warp counts. Chunk 0 also
+// publishes counts, offsets, the active experts and their number.
+__global__ void __launch_bounds__(256) bucket_place_kernel(const int* __restrict__ idx, int n_slots, int n_exp,
+                                                           const int* __restrict__ ghist, int n_chunks,
+                                                           int* __restrict__ counts, int* __restrict__ offsets,
+                                                           int* __restrict__ active, int* __restrict__ n_active,
+                                                           int* __restrict__ perm, int* __restrict__ rowof) {
+  __shared__ int run[256];        // next position of each expert for this chunk
+  __shared__ int wcnt[8][256];    // slots of each expert per warp in the current round
+  __shared__ int scan_w[8], scan_a[8];
+  const int e = threadIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int tot = 0, pre = 0;
+  if (e < n_exp)
+    for (int b = 0; b < n_chunks; ++b) {
+      const int c = ghist[(size_t)b * n_exp + e];
       tot += c;
+      if (b < (int)blockIdx.x) pre += c;
     }
-    if (hit) {
-      const int pos = running + before + __popc(m & ((1u << lane) - 1u));
-      perm[pos] = i;
-      rowof[i] = pos;
+  // exclusive scans over the experts of the totals and of the active flags (block-wide)
+  int inc = tot, inca = tot > 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o), va = __shfl_up_sync(0xffffffffu, inca, o);
+    if (lane >= o) { inc += v; inca += va; }
+  }
+  if (lane == 31) { scan_w[warp] = inc; scan_a[warp] = inca; }
+  __syncthreads();
+  int wbase = 0, abase = 0, all = 0, all_a = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) { wbase += scan_w[w]; abase += scan_a[w]; }
+    all += scan_w[w];
+    all_a += scan_a[w];
+  }
+  const int off = wbase + inc - tot;  // exclusive
+  if (e < n_exp) {
+    run[e] = off + pre;
+    if (blockIdx.x == 0) {
+      counts[e] = tot;
+      offsets[e] = off;
+      if (tot > 0) active[abase + inca - 1] = e;
     }
-    running += tot;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    offsets[n_exp] = all;
+    *n_active = all_a;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  const int s0 = blockIdx.x * kChunk;
+  for (int r0 = 0; r0 < kChunk; r0 += 256) {
+    for (int k = threadIdx.x; k < 8 * 256; k += 256) (&wcnt[0][0])[k] = 0;
+    __syncthreads();
+    const int sl = s0 + r0 + threadIdx.x;
+    const int ex = sl < n_slots ? idx[sl] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, ex);
+    const int rank = __popc(m & lt);
+    if (ex >= 0 && rank == 0) wcnt[warp][ex] = __popc(m);
+    __syncthreads();
+    if (ex >= 0) {
+      int pos = run[ex] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w][ex];
+      perm[pos] = sl;
+      rowof[sl] = pos;
+    }
+    __syncthreads();
+    if (e < n_exp) {
+      int add = 0;
+      for (int w = 0; w < 8; ++w) add += wcnt[w][e];
+      run[e] += add;
+    }
+    __syncthreads();
   }
 }
 
@@ -197,13 +218,17 @@ void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const
       logits, n_learned, n_exp, top_k, token_ids, n_hash, table, vocab, idx, wts, err);
 }
 
-void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* counts, cudaStream_t s) {
-  bucket_count_kernel<<<n_exp, 256, 0, s>>>(idx, n_slots, counts);
+int bucket_chunks(int n_slots) { return (n_slots + kChunk - 1) / kChunk; }
+
+void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* ghist, cudaStream_t s) {
+  bucket_hist_kernel<<<bucket_chunks(n_slots), 256, 0, s>>>(idx, n_slots, n_exp, ghist);
 }
 
-void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* counts, int* offsets, int* active,
-                           int* n_active, int* perm, int* rowof, cudaStream_t s) {
-  bucket_scatter_kernel<<<n_exp, 256, 0, s>>>(idx, n_slots, n_exp, counts, offsets, active, n_active, perm, rowof);
+void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, int* counts, int* offsets,
+                           int* active, int* n_active, int* perm, int* rowof, cudaStream_t s) {
+  const int nc = bucket_chunks(n_slots);
+  bucket_place_kernel<<<nc, 256, 0, s>>>(idx, n_slots, n_exp, ghist, nc, counts, offsets, active, n_active, perm,
+                                         rowof);
 }
 
 }  // namespace ds4
