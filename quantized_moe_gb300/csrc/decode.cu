@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
       float m = 0.f;
       for (int w = 0; w < kWarps; ++w) m = fmaxf(m, xmx[w][t]);
       a.xmax[t] = m;
+      a.xscale[t] = fp16_row_scale(m);  // final once this grid completes
     }
   }
   // ---- arrival: the last CTA continues with the top-k and the bucketing. The barrier orders the
@@ -96,6 +97,57 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   if (!s_last) return;
   const int K = a.top_k, E = a.n_exp, n_slots = nt * K;
   if (threadIdx.x == 0) *a.err = 0;  // only this CTA writes the error word
+  if (nt == 1 && a.n_hash == 0) {
+    // One learned token: thread e ranks expert e among all (higher score first, ties to the
+    // lower index: the order of the warp selection below), and the k winners are bucketed in
+    // closed form (one position each, in ascending expert id).
+    __shared__ float s_sc[256], s_selw[16];
+    __shared__ int s_sel[16];
+    const int ex = threadIdx.x;
+    const float sc = ex < E ? 1.f / (1.f + expf(-__ldcg(a.logits + ex))) : -1.f;
+    s_sc[ex] = sc;
+    __syncthreads();
+    int rank = 0;
+    if (ex < E) {
+#pragma unroll 8
+      for (int j = 0; j < E; ++j) {
+        const float v = s_sc[j];
+        rank += (v > sc) || (v == sc && j < ex);
+      }
+      if (rank < K) {
+        s_sel[rank] = ex;
+        s_selw[rank] = sc;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < K) {
+      const int r = threadIdx.x, er = s_sel[r];
+      float sum = 0.f;
+      for (int q = 0; q < K; ++q) sum += s_selw[q];  // selection order, as the warp version
+      int pos = 0;
+      for (int q = 0; q < K; ++q) pos += s_sel[q] < er;
+      a.idx[r] = er;
+      a.wts[r] = s_selw[r] / sum;
+      a.perm[pos] = r;
+      a.rowof[r] = pos;
+      a.tokof[pos] = 0;
+      a.active[pos] = er;
+      a.work[pos] = make_int4(er, pos, 1, 1);
+    }
+    if (ex < E) {
+      int off = 0;
+      for (int q = 0; q < K; ++q) off += s_sel[q] < ex;
+      a.counts[ex] = rank < K ? 1 : 0;
+      a.offsets[ex] = off;
+    }
+    if (threadIdx.x == 0) {
+      a.offsets[E] = K;
+      *a.n_active = K;
+    }
+    for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
+    if (threadIdx.x == 0) *a.counter = 0u;
+    return;
+  }
   for (int t = warp; t < nt; t += kWarps) {
     if (t < a.n_hash) {
       const int id = a.token_ids[t];
@@ -197,7 +249,6 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
     a.rowof[sl] = pos;
     a.tokof[pos] = sl / K;
   }
-  for (int t = threadIdx.x; t < nt; t += kThreads) a.xscale[t] = fp16_row_scale(__ldcg(a.xmax + t));
   for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
   if (threadIdx.x == 0) *a.counter = 0u;  // every CTA has arrived: ready for the next forward
 }
