@@ -87,9 +87,35 @@ __device__ __forceinline__ uint32_t a_row_addr(uint32_t a_base, int rg16, int sb
   return a_base + (row >> 3) * 1024 + (row & 7) * 128 + ((kc ^ (row & 7)) << 4);
 }
 
+// Two 16-k sub-blocks I0, I0 + 1 of a Q2_K chunk for this lane's rows g, g+8: every shift is a
+// constant (the field of sub-block 4 is already at mantissa bits 8-9).
+template <int I0>
+__device__ __forceinline__ void deq_q2k_pair(const uint32_t (&w)[4], uint32_t scw, __half2 d2, __half2 ndm2,
+                                             __half2 dm1024, uint32_t a_base, const uint32_t (&aoff)[2]) {
+  const __half2 k1024 = __float2half2_rn(1024.f);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    constexpr int kSh0 = 8 - 2 * I0;  // left shift of sub-block I0 (negative: right)
+    const int sh = kSh0 - 2 * j;
+    const uint32_t sc = scw >> (8 * j);
+    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), d2);  // 2^16 d s, rounded once
+    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), ndm2, dm1024);  // -dmin m
+    uint32_t a[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      // the quant pair moved to mantissa bits 8-9: the exact fp16 subnormal q * 2^-16, so one
+      // FMA with 2^16 d s gives d s q - dmin m with a single rounding
+      const uint32_t qb = (sh >= 0 ? (w[r] << sh) : (w[r] >> -sh)) & 0x03000300u;
+      a[r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
+                         : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
+    }
+    stmatrix_x4(a_base + aoff[j], a[0], a[1], a[2], a[3]);
+  }
+}
+
 // Dequantize half (32 k: two 16-k sub-blocks) of the 16 rows x 64 k of one Q2_K unit that fall in
 // K stage su (0..3) and store them.
-__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int rg16, int half) {
+__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2]) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const int c = su >> 1, i0 = (su & 1) * 4 + 2 * half;  // first sub-block of the chunk handled here
   const uint4 qw = lds128(unit + c * 512 + 16 * lane);
@@ -105,30 +131,18 @@ __device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, 
   // m is read as the fp16 1024 + m; one FMA with -dmin and 1024 dmin (exact: a power of two)
   // then gives -dmin * m rounded once
   const __half2 ndm2 = __hneg2(dm2);
-  const __half2 k1024 = __float2half2_rn(1024.f);
-  const __half2 dm1024 = __hmul2(dm2, k1024);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = i0 + j;
-    const uint32_t sc = scw >> (8 * j);
-    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), d2);  // 2^16 d s, rounded once
-    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), ndm2, dm1024);  // -dmin m
-    uint32_t a[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      // the quant pair moved to mantissa bits 8-9: the exact fp16 subnormal q * 2^-16, so one
-      // FMA with 2^16 d s gives d s q - dmin m with a single rounding
-      const uint32_t qb = (i < 4 ? (w[r] << (8 - 2 * i)) : (w[r] >> (2 * i - 8))) & 0x03000300u;
-      a[r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
-                         : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
-    }
-    stmatrix_x4(a_row_addr(a_base, rg16, 2 * half + j), a[0], a[1], a[2], a[3]);
+  const __half2 dm1024 = __hmul2(dm2, __float2half2_rn(1024.f));
+  switch (i0) {  // uniform across the warp
+    case 0: deq_q2k_pair<0>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
+    case 2: deq_q2k_pair<2>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
+    case 4: deq_q2k_pair<4>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
+    default: deq_q2k_pair<6>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
   }
 }
 
 // Dequantize half (two 16-k sub-blocks) of the 16 rows x 64 k of one Q8_0 unit (128 k) that fall
 // in K stage su (0..1).
-__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int rg16, int half) {
+__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2]) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const __half2 k1152 = __float2half2_rn(1152.f);
 #pragma unroll
@@ -144,7 +158,7 @@ __device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, 
 #pragma unroll
     for (int r = 0; r < 4; ++r)
       a[r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? __high2half2(sc) : __low2half2(sc)));
-    stmatrix_x4(a_row_addr(a_base, rg16, ii), a[0], a[1], a[2], a[3]);
+    stmatrix_x4(a_base + aoff[j], a[0], a[1], a[2], a[3]);
   }
 }
 
@@ -320,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     // ------------------------------------------------------------------ dequant
     const int dw = warp - kFirstDeq;
     const int rgw = dw & 7, half = dw >> 3;  // 16-row group of the slice, half of each K stage
+    // this lane's stmatrix row offsets for the warp's two sub-blocks of a stage (fixed per warp)
+    const uint32_t aoff[2] = {a_row_addr(0, rgw, 2 * half), a_row_addr(0, rgw, 2 * half + 1)};
     uint32_t gs = 0;
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
@@ -332,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
         if (FMT == FMT_Q2_K)
-          deq_q2k(unit, su, a_base, rgw, half);
+          deq_q2k(unit, su, a_base, half, aoff);
         else
-          deq_q80(unit, su, a_base, rgw, half);
+          deq_q80(unit, su, a_base, half, aoff);
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
         if (lane == 0) {
