@@ -113,30 +113,40 @@ __device__ __forceinline__ void deq_q2k_pair(const uint32_t (&w)[4], uint32_t sc
   }
 }
 
+// Per-row constants of a Q2_K unit for this lane's rows (g, g+8): 2^16 d (exact: only the exponent
+// changes; create refuses super-blocks whose 2^16 d * 15 would leave the fp16 range), -dmin and
+// 1024 dmin (m is read as the fp16 1024 + m, so one FMA gives -dmin * m rounded once).
+struct Q2kRowConst {
+  __half2 d2, ndm2, dm1024;
+};
+
+__device__ __forceinline__ Q2kRowConst q2k_row_const(uint32_t unit) {
+  const int g = (threadIdx.x & 31) >> 2;
+  const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
+  const __half2 k256 = __float2half2_rn(256.f);
+  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));  // (dmin of row g, dmin of row g+8)
+  Q2kRowConst r;
+  r.d2 = __hmul2(__hmul2(u2h(prmt(dd0, dd1, 0x5410u)), k256), k256);
+  r.ndm2 = __hneg2(dm2);
+  r.dm1024 = __hmul2(dm2, __float2half2_rn(1024.f));
+  return r;
+}
+
 // Dequantize half (32 k: two 16-k sub-blocks) of the 16 rows x 64 k of one Q2_K unit that fall in
 // K stage su (0..3) and store them.
-__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2]) {
+__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2],
+                                        const Q2kRowConst& rc) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const int c = su >> 1, i0 = (su & 1) * 4 + 2 * half;  // first sub-block of the chunk handled here
   const uint4 qw = lds128(unit + c * 512 + 16 * lane);
   const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
   // scale bytes of sub-blocks i0, i0 + 1: byte 0/1 row g, byte 2/3 row g + 8
   const uint32_t scw = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
-  const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
-  // (d of row g, d of row g+8) times 2^16: exact (only the exponent changes); create refuses
-  // super-blocks whose d * 15 * 2^16 would leave the fp16 range
-  const __half2 k256 = __float2half2_rn(256.f);
-  const __half2 d2 = __hmul2(__hmul2(u2h(prmt(dd0, dd1, 0x5410u)), k256), k256);
-  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));  // (dmin of row g, dmin of row g+8)
-  // m is read as the fp16 1024 + m; one FMA with -dmin and 1024 dmin (exact: a power of two)
-  // then gives -dmin * m rounded once
-  const __half2 ndm2 = __hneg2(dm2);
-  const __half2 dm1024 = __hmul2(dm2, __float2half2_rn(1024.f));
   switch (i0) {  // uniform across the warp
-    case 0: deq_q2k_pair<0>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
-    case 2: deq_q2k_pair<2>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
-    case 4: deq_q2k_pair<4>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
-    default: deq_q2k_pair<6>(w, scw, d2, ndm2, dm1024, a_base, aoff); break;
+    case 0: deq_q2k_pair<0>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
+    case 2: deq_q2k_pair<2>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
+    case 4: deq_q2k_pair<4>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
+    default: deq_q2k_pair<6>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
   }
 }
 
@@ -336,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     const int rgw = dw & 7, half = dw >> 3;  // 16-row group of the slice, half of each K stage
     // this lane's stmatrix row offsets for the warp's two sub-blocks of a stage (fixed per warp)
     const uint32_t aoff[2] = {a_row_addr(0, rgw, 2 * half), a_row_addr(0, rgw, 2 * half + 1)};
+    Q2kRowConst rc{};  // constants of the current unit (Q2_K), refreshed when a unit starts
     uint32_t gs = 0;
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
@@ -347,9 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         if (!mbar_wait(&b.a_empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
-        if (FMT == FMT_Q2_K)
-          deq_q2k(unit, su, a_base, half, aoff);
-        else
+        if (FMT == FMT_Q2_K) {
+          if (su == 0) rc = q2k_row_const(unit);
+          deq_q2k(unit, su, a_base, half, aoff, rc);
+        } else
           deq_q80(unit, su, a_base, half, aoff);
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
