@@ -28,30 +28,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ id
     for (int j = 0; j < top_k; ++j) { s_pos[j] = p[j]; s_w[j] = w[j]; }
   }
   __syncthreads();
-  const int i4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i4 >= d) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < top_k; ++j) {
-    const float4 v = *reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4);
-    const float w = s_w[j];
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  for (int i4 = threadIdx.x * 4; i4 < d; i4 += blockDim.x * 4) {  // the whole row: one sort per token
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < top_k; ++j) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4));  // read once
+      const float w = s_w[j];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (ys) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(ys + (size_t)t * d + i4));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    __stcs(reinterpret_cast<float4*>(out + (size_t)t * d + i4), acc);
   }
-  if (ys) {
-    const float4 v = *reinterpret_cast<const float4*>(ys + (size_t)t * d + i4);
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-  }
-  *reinterpret_cast<float4*>(out + (size_t)t * d + i4) = acc;
 }
 
 }  // namespace
 
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s) {
-  dim3 grid((d / 4 + 255) / 256, n_tok);
-  combine_kernel<<<grid, 256, 0, s>>>(idx, wts, rowof, y, ys, top_k, d, out);
+  combine_kernel<<<dim3(1, n_tok), 256, 0, s>>>(idx, wts, rowof, y, ys, top_k, d, out);
 }
 
 }  // namespace ds4

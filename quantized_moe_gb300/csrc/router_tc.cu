@@ -6,14 +6,16 @@
 // step go into a fresh fp32 accumulator, which is added to the running sum with ordinary fp32
 // adds: the accuracy of fp32 FMAs on the CUDA cores, at tensor-core throughput.
 //
-// CTA = 64 tokens x 64 experts, 4 warps (16 tokens each, all 64 experts); K staged through
-// shared memory 32 at a time, double-buffered with cp.async.
+// CTA = 64 tokens x 64 experts, 16 warps (each 16 tokens x 16 experts: enough warps per SM to
+// hide the MMA -> add chains); K staged through shared memory 32 at a time, double-buffered with
+// cp.async.
 #include "common.cuh"
 
 namespace ds4 {
 namespace {
 
 constexpr int TT = 64, TE = 64, KS = 32;
+constexpr int kThreads = 512;  // 16 warps: 4 token groups x 4 expert groups
 constexpr int PAD = 8;  // bf16 elements of padding per shared row (keeps ldmatrix conflict-free)
 constexpr int LDS = KS + PAD;
 
@@ -43,7 +45,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 // w3: [3][E][d] bf16 parts of the router weights
-__global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
+__global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
                                                         const __nv_bfloat16* __restrict__ w3, const float* __restrict__ b,
                                                         int n_exp, float* __restrict__ logits) {
   __shared__ __align__(16) __nv_bfloat16 xs[2][TT][LDS];
@@ -52,8 +54,8 @@ __global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __r
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t plane = (size_t)n_exp * d;
   auto stage = [&](int buf, int k0) {
-    // 64 rows x 32 k = 256 chunks of 16 bytes for x, 3 x 256 for the weight parts; 128 threads
-    for (int c = threadIdx.x; c < 4 * TT * (KS / 8); c += 128) {
+    // 64 rows x 32 k = 256 chunks of 16 bytes for x, 3 x 256 for the weight parts
+    for (int c = threadIdx.x; c < 4 * TT * (KS / 8); c += kThreads) {
       const int which = c / (TT * (KS / 8)), r = (c / (KS / 8)) % TT, kc = c % (KS / 8);
       if (which == 0) {
         const int t = t0 + r;
@@ -66,9 +68,10 @@ __global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __r
     }
     cp_async_commit();
   };
-  float acc[TE / 8][4];
+  const int tw = warp & 3, ew = warp >> 2;  // token group (16 tokens), expert group (16 experts)
+  float acc[2][4];
 #pragma unroll
-  for (int j = 0; j < TE / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
   const int n_k = d / KS;
   stage(0, 0);
   for (int ks = 0; ks < n_k; ++ks) {
@@ -84,18 +87,18 @@ __global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __r
     for (int kk = 0; kk < KS; kk += 16) {
       uint32_t a[4];
       {  // A: 16 tokens x 16 k of this warp (row-major)
-        const int r = warp * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
+        const int r = tw * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
         ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[buf][r][c])), a[0], a[1], a[2], a[3]);
       }
 #pragma unroll
-      for (int j = 0; j < TE / 8; ++j) {
+      for (int j = 0; j < 2; ++j) {
         // The tensor core's accumulation truncates; a long chain of MMAs into one accumulator
         // would bias the sum. Each 16-wide K step therefore starts from zero and is added to
         // the running fp32 sum with round-to-nearest adds.
         float tmp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int part = 0; part < 3; ++part) {  // B: 8 experts x 16 k (expert rows, k contiguous)
-          const int r = j * 8 + (lane & 7), c = kk + ((lane >> 3) & 1) * 8;
+          const int r = ew * 16 + j * 8 + (lane & 7), c = kk + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1;
           ldmatrix_x2(static_cast<uint32_t>(__cvta_generic_to_shared(&ws[buf][part][r][c])), b0, b1);
           mma_bf16_16816(tmp, a, b0, b1);
@@ -109,10 +112,10 @@ __global__ void __launch_bounds__(128) router_tc_kernel(const __nv_bfloat16* __r
   // C fragment: rows g, g+8 (tokens), columns 2t, 2t+1 (experts)
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int j = 0; j < TE / 8; ++j)
+  for (int j = 0; j < 2; ++j)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int tok = t0 + warp * 16 + g + 8 * (c >> 1), e = e0 + j * 8 + 2 * t + (c & 1);
+      const int tok = t0 + tw * 16 + g + 8 * (c >> 1), e = e0 + ew * 16 + j * 8 + 2 * t + (c & 1);
       if (tok < n_tok && e < n_exp) logits[(size_t)tok * n_exp + e] = acc[j][c] + (b ? b[e] : 0.f);
     }
 }
@@ -140,7 +143,7 @@ void launch_router_split(const float* w, size_t n, __nv_bfloat16* w3, cudaStream
 void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
                       float* logits, cudaStream_t s) {
   dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
-  router_tc_kernel<<<grid, 128, 0, s>>>(x, n_tok, d, w3, b, n_exp, logits);
+  router_tc_kernel<<<grid, kThreads, 0, s>>>(x, n_tok, d, w3, b, n_exp, logits);
 }
 
 }  // namespace ds4
