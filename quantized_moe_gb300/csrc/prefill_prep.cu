@@ -44,16 +44,31 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
   if (threadIdx.x == 0) inv_s[t] = 1.f / sc;
 }
 
-// One CTA per bucketed position: copy the token's fp16 row.
+// One warp per bucketed position: copy the token's fp16 row; each lane issues eight 16-byte loads
+// before its stores, so a warp keeps 4 KB in flight.
 __global__ void __launch_bounds__(256) gather_kernel(const __half* __restrict__ xs16, const float* __restrict__ inv_s,
-                                                     const int* __restrict__ perm, int top_k, int d,
+                                                     const int* __restrict__ perm, int n_slots, int top_k, int d,
                                                      __half* __restrict__ xp16, float* __restrict__ inv_p) {
-  const int pos = blockIdx.x;
+  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (pos >= n_slots) return;
   const int tok = perm[pos] / top_k;
   const uint4* src = reinterpret_cast<const uint4*>(xs16 + (size_t)tok * d);
   uint4* dst = reinterpret_cast<uint4*>(xp16 + (size_t)pos * d);
-  for (int i = threadIdx.x; i < d / 8; i += 256) dst[i] = src[i];
-  if (threadIdx.x == 0) inv_p[pos] = inv_s[tok];
+  const int n16 = d / 8;
+  for (int i0 = 0; i0 < n16; i0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 + lane;
+      if (i < n16) v[u] = src[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 + lane;
+      if (i < n16) __stcs(dst + i, v[u]);
+    }
+  }
+  if (lane == 0) inv_p[pos] = inv_s[tok];
 }
 
 // One thread per expert: ceil(count / tile_n) tiles, placed by an exclusive scan over experts.
@@ -91,7 +106,7 @@ void launch_xprep(const __nv_bfloat16* x, int n_tok, int d, __half* xs16, float*
 
 void launch_gather(const __half* xs16, const float* inv_s, const int* perm, int n_slots, int top_k, int d,
                    __half* xp16, float* inv_p, cudaStream_t s) {
-  gather_kernel<<<n_slots, 256, 0, s>>>(xs16, inv_s, perm, top_k, d, xp16, inv_p);
+  gather_kernel<<<(n_slots + 7) / 8, 256, 0, s>>>(xs16, inv_s, perm, n_slots, top_k, d, xp16, inv_p);
 }
 
 void launch_tiles(const int* counts, const int* offsets, int n_exp, int tile_n, int4* tiles, int* n_tiles,

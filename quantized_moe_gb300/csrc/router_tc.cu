@@ -7,8 +7,8 @@
 // adds: the accuracy of fp32 FMAs on the CUDA cores, at tensor-core throughput.
 //
 // CTA = 64 tokens x 64 experts, 16 warps (each 16 tokens x 16 experts: enough warps per SM to
-// hide the MMA -> add chains); K staged through shared memory 32 at a time, double-buffered with
-// cp.async.
+// hide the MMA -> add chains); K staged through shared memory 32 at a time in a four-deep
+// cp.async pipeline (three steps of loads in flight).
 #include "common.cuh"
 
 namespace ds4 {
@@ -18,6 +18,12 @@ constexpr int TT = 64, TE = 64, KS = 32;
 constexpr int kThreads = 512;  // 16 warps: 4 token groups x 4 expert groups
 constexpr int PAD = 8;  // bf16 elements of padding per shared row (keeps ldmatrix conflict-free)
 constexpr int LDS = KS + PAD;
+constexpr int NSTAGE = 4;
+struct Stage {
+  __nv_bfloat16 x[TT][LDS];
+  __nv_bfloat16 w[3][TE][LDS];
+};
+constexpr int kSmem = NSTAGE * (int)sizeof(Stage);
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool pred) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -25,8 +31,8 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool pred
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(sz) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -48,8 +54,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 __global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
                                                         const __nv_bfloat16* __restrict__ w3, const float* __restrict__ b,
                                                         int n_exp, float* __restrict__ logits) {
-  __shared__ __align__(16) __nv_bfloat16 xs[2][TT][LDS];
-  __shared__ __align__(16) __nv_bfloat16 ws[2][3][TE][LDS];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Stage* st = reinterpret_cast<Stage*>(smem_raw);
   const int t0 = blockIdx.x * TT, e0 = blockIdx.y * TE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t plane = (size_t)n_exp * d;
@@ -59,10 +65,10 @@ __global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16
       const int which = c / (TT * (KS / 8)), r = (c / (KS / 8)) % TT, kc = c % (KS / 8);
       if (which == 0) {
         const int t = t0 + r;
-        cp_async16(&xs[buf][r][kc * 8], x + (size_t)min(t, n_tok - 1) * d + k0 + kc * 8, t < n_tok);
+        cp_async16(&st[buf].x[r][kc * 8], x + (size_t)min(t, n_tok - 1) * d + k0 + kc * 8, t < n_tok);
       } else {
         const int e = e0 + r;
-        cp_async16(&ws[buf][which - 1][r][kc * 8], w3 + (which - 1) * plane + (size_t)min(e, n_exp - 1) * d + k0 + kc * 8,
+        cp_async16(&st[buf].w[which - 1][r][kc * 8], w3 + (which - 1) * plane + (size_t)min(e, n_exp - 1) * d + k0 + kc * 8,
                    e < n_exp);
       }
     }
@@ -73,22 +79,27 @@ __global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16
 #pragma unroll
   for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
   const int n_k = d / KS;
-  stage(0, 0);
+  for (int s0 = 0; s0 < NSTAGE - 1; ++s0) {
+    if (s0 < n_k)
+      stage(s0, s0 * KS);
+    else
+      cp_async_commit();  // empty group: the group count stays in step
+  }
   for (int ks = 0; ks < n_k; ++ks) {
-    const int buf = ks & 1;
-    if (ks + 1 < n_k) {
-      stage(buf ^ 1, (ks + 1) * KS);
-      cp_async_wait1();
-    } else {
-      cp_async_wait0();
-    }
-    __syncthreads();
+    const int buf = ks % NSTAGE;
+    cp_async_wait<NSTAGE - 2>();  // step ks has landed (for this thread)
+    __syncthreads();              // ... for every thread, and step ks - 1's buffer is free again
+    const int nxt = ks + NSTAGE - 1;
+    if (nxt < n_k)
+      stage(nxt % NSTAGE, nxt * KS);
+    else
+      cp_async_commit();
 #pragma unroll
     for (int kk = 0; kk < KS; kk += 16) {
       uint32_t a[4];
       {  // A: 16 tokens x 16 k of this warp (row-major)
         const int r = tw * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
-        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&xs[buf][r][c])), a[0], a[1], a[2], a[3]);
+        ldmatrix_x4(static_cast<uint32_t>(__cvta_generic_to_shared(&st[buf].x[r][c])), a[0], a[1], a[2], a[3]);
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -100,15 +111,15 @@ __global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16
         for (int part = 0; part < 3; ++part) {  // B: 8 experts x 16 k (expert rows, k contiguous)
           const int r = ew * 16 + j * 8 + (lane & 7), c = kk + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1;
-          ldmatrix_x2(static_cast<uint32_t>(__cvta_generic_to_shared(&ws[buf][part][r][c])), b0, b1);
+          ldmatrix_x2(static_cast<uint32_t>(__cvta_generic_to_shared(&st[buf].w[part][r][c])), b0, b1);
           mma_bf16_16816(tmp, a, b0, b1);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[j][c] += tmp[c];
       }
     }
-    __syncthreads();
   }
+  cp_async_wait<0>();
   // C fragment: rows g, g+8 (tokens), columns 2t, 2t+1 (experts)
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -143,7 +154,12 @@ void launch_router_split(const float* w, size_t n, __nv_bfloat16* w3, cudaStream
 void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
                       float* logits, cudaStream_t s) {
   dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
-  router_tc_kernel<<<grid, kThreads, 0, s>>>(x, n_tok, d, w3, b, n_exp, logits);
+  static bool attr_set = false;  // per process; the attribute belongs to the function
+  if (!attr_set) {
+    cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    attr_set = true;
+  }
+  router_tc_kernel<<<grid, kThreads, kSmem, s>>>(x, n_tok, d, w3, b, n_exp, logits);
 }
 
 }  // namespace ds4
