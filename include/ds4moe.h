@@ -123,7 +123,9 @@ int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n_tokens, const i
                       int32_t n_hash, float* out, void* stream);
 
 /* As ds4moe_forward_ex with host buffers: copies x (and token_ids) to the device, runs the
- * forward and copies out back, then synchronises the stream before returning. */
+ * forward and copies out back, then synchronises the stream before returning. With page-locked
+ * host buffers and a decode-sized batch, the copies and the kernels replay as one cached CUDA
+ * graph (keyed by the buffer addresses); pageable buffers take separate copies. */
 int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t n_tokens,
                         const int32_t* token_ids_host, int32_t n_hash, float* out_host, void* stream);
 

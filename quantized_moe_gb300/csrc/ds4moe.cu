@@ -141,15 +141,27 @@ struct ds4moe_handle {
     const void* x = nullptr;
     const int* tid = nullptr;
     float* out = nullptr;
+    // host entry point: pinned host buffers copied inside the graph (null for device forwards)
+    const void* hx = nullptr;
+    const int* htid = nullptr;
+    float* hout = nullptr;
     cudaGraphExec_t exec = nullptr;
     uint64_t used = 0;
   };
+  struct HostIo {
+    const void* x = nullptr;
+    const int* tid = nullptr;
+    float* out = nullptr;
+  };
+  static constexpr int kPinned = 16;
+  const void* pinned[kPinned] = {};  // host addresses known to be page-locked
+  int pinned_next = 0;
   static constexpr int kGraphs = 16;
   GraphEntry graphs[kGraphs];
   uint64_t tick = 0;
 
   int decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int n_hash, float* out,
-                   cudaGraphExec_t* exec_out);
+                   cudaGraphExec_t* exec_out, const HostIo* io = nullptr);
   void release_graphs() {
     for (GraphEntry& g : graphs)
       if (g.exec) {
@@ -195,11 +207,14 @@ struct ds4moe_handle {
 };
 
 int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int nh, float* o,
-                                cudaGraphExec_t* exec_out) {
+                                cudaGraphExec_t* exec_out, const HostIo* io) {
+  const HostIo hio = io ? *io : HostIo();
   GraphEntry* hit = nullptr;
   GraphEntry* victim = &graphs[0];
   for (GraphEntry& g : graphs) {
-    if (g.exec && g.n == da.n_tok && g.n_hash == nh && g.x == x && g.tid == tid && g.out == o) hit = &g;
+    if (g.exec && g.n == da.n_tok && g.n_hash == nh && g.x == x && g.tid == tid && g.out == o && g.hx == hio.x &&
+        g.htid == hio.tid && g.hout == hio.out)
+      hit = &g;
     if (!g.exec || g.used < victim->used) victim = &g;
   }
   if (!hit) {
@@ -210,7 +225,15 @@ int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const 
     }
     cudaGraph_t graph = nullptr;
     DS4_CUDA(cudaStreamBeginCapture(cap_stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, true, cap_stream, nullptr, nullptr);
+    const size_t d = (size_t)s.d;
+    cudaError_t e = cudaSuccess;
+    if (hio.x) e = cudaMemcpyAsync(const_cast<void*>(x), hio.x, (size_t)da.n_tok * d * 2, cudaMemcpyHostToDevice, cap_stream);
+    if (e == cudaSuccess && hio.tid && nh > 0)
+      e = cudaMemcpyAsync(const_cast<int*>(tid), hio.tid, (size_t)nh * 4, cudaMemcpyHostToDevice, cap_stream);
+    if (e == cudaSuccess)
+      e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, true, cap_stream, nullptr, nullptr);
+    if (e == cudaSuccess && hio.out)
+      e = cudaMemcpyAsync(hio.out, o, (size_t)da.n_tok * d * 4, cudaMemcpyDeviceToHost, cap_stream);
     cudaError_t e2 = cudaStreamEndCapture(cap_stream, &graph);
     if (e != cudaSuccess || e2 != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -226,6 +249,9 @@ int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const 
     victim->x = x;
     victim->tid = tid;
     victim->out = o;
+    victim->hx = hio.x;
+    victim->htid = hio.tid;
+    victim->hout = hio.out;
     victim->exec = exec;
     hit = victim;
   }
@@ -498,6 +524,41 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   return DS4MOE_OK;
 }
 
+// Arguments of the decode kernels for one forward over the handle's workspace.
+ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, int n, const int32_t* token_ids, int n_hash,
+                            float* out) {
+  const ds4moe_shapes& s = h->s;
+  ds4::DecodeArgs da{};
+  da.x = xb; da.n_tok = n; da.d = s.d; da.wr = h->router_w; da.br = h->router_b; da.n_exp = s.n_experts;
+  da.top_k = s.top_k; da.token_ids = token_ids; da.n_hash = n_hash; da.table = h->table; da.vocab = s.hash_vocab;
+  da.logits = h->logits; da.xmax = h->xmax; da.idx = h->idx; da.wts = h->wts; da.counts = h->counts;
+  da.offsets = h->offsets; da.active = h->active; da.n_active = h->n_active; da.perm = h->perm;
+  da.rowof = h->rowof; da.err = h->err; da.counter = h->counter; da.hmax = h->hmax;
+  da.work = h->work; da.tokof = h->tokof; da.xscale = h->xscale;
+  da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = s.f_routed;
+  da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
+  da.fs = s.f_shared; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
+  return da;
+}
+
+bool is_decode(const ds4moe_handle* h, int n) {
+  return n <= ds4::decode_max_tokens() && n * h->s.top_k <= ds4::decode_max_slots();
+}
+
+// Host memory that is page-locked (a graph may copy from and to it); remembered per handle.
+bool host_pinned(ds4moe_handle* h, const void* p) {
+  for (const void* q : h->pinned)
+    if (q == p) return true;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type != cudaMemoryTypeHost) return false;
+  h->pinned[h->pinned_next++ % ds4moe_handle::kPinned] = p;
+  return true;
+}
+
 extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, const int32_t* token_ids,
                                  int32_t n_hash, float* out, void* stream) {
   if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
@@ -539,16 +600,7 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   };
   if (n <= ds4::decode_max_tokens() && n * K <= ds4::decode_max_slots()) {
     // decode path: three kernels, chained with programmatic dependent launch unless profiling
-    ds4::DecodeArgs da{};
-    da.x = xb; da.n_tok = n; da.d = d; da.wr = h->router_w; da.br = h->router_b; da.n_exp = E; da.top_k = K;
-    da.token_ids = token_ids; da.n_hash = n_hash; da.table = h->table; da.vocab = s.hash_vocab;
-    da.logits = h->logits; da.xmax = h->xmax; da.idx = h->idx; da.wts = h->wts; da.counts = h->counts;
-    da.offsets = h->offsets; da.active = h->active; da.n_active = h->n_active; da.perm = h->perm;
-    da.rowof = h->rowof; da.err = h->err; da.counter = h->counter; da.hmax = h->hmax;
-    da.work = h->work; da.tokof = h->tokof; da.xscale = h->xscale;
-    da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = f;
-    da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
-    da.fs = fs; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
+    const ds4::DecodeArgs da = decode_args(h, xb, n, token_ids, n_hash, out);
     struct Ctx {
       decltype(mark)* m;
     } ctx{&mark};
@@ -639,10 +691,35 @@ extern "C" int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t
     return fail(n < 0 ? DS4MOE_ERR_INVALID_ARG : DS4MOE_ERR_CAPACITY, "n_tokens=%d outside 0..max_tokens=%d", n, h->s.max_tokens);
   if (n == 0) return DS4MOE_OK;
   if (!x_host || !out_host || (n_hash > 0 && !tid_host)) return fail(DS4MOE_ERR_INVALID_ARG, "x, out or token_ids is NULL");
+  if (n_hash < 0 || n_hash > n) return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d must be in 0..n_tokens", n_hash);
+  if (n_hash > 0 && h->s.hash_vocab == 0)
+    return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d needs a handle with a hash table and token_ids", n_hash);
   DeviceGuard guard(h->s.device);
   if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", h->s.device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t d = (size_t)h->s.d;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DS4_CUDA(cudaStreamIsCapturing(st, &cap));
+  if (is_decode(h, n) && h->use_graphs && !h->profile && cap == cudaStreamCaptureStatusNone &&
+      host_pinned(h, x_host) && host_pinned(h, out_host) &&
+      (n_hash == 0 || host_pinned(h, tid_host))) {
+    // one graph: host -> device copies, the decode kernels, device -> host copy
+    const ds4::DecodeArgs da = decode_args(h, reinterpret_cast<const __nv_bfloat16*>(h->x_stage), n,
+                                           n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage);
+    ds4moe_handle::HostIo io;
+    io.x = x_host;
+    io.tid = n_hash > 0 ? tid_host : nullptr;
+    io.out = out_host;
+    cudaGraphExec_t exec = nullptr;
+    int rc = h->decode_graph(da, h->x_stage, n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage, &exec, &io);
+    if (rc != DS4MOE_OK) return rc;
+    DS4_CUDA(cudaGraphLaunch(exec, st));
+    DS4_CUDA(cudaStreamSynchronize(st));
+    h->n_phases = 0;
+    h->last_stream = st;
+    h->last_n = n;
+    return DS4MOE_OK;
+  }
   DS4_CUDA(cudaMemcpyAsync(h->x_stage, x_host, (size_t)n * d * 2, cudaMemcpyHostToDevice, st));
   if (n_hash > 0) DS4_CUDA(cudaMemcpyAsync(h->tid_stage, tid_host, (size_t)n_hash * 4, cudaMemcpyHostToDevice, st));
   int rc = ds4moe_forward_ex(h, h->x_stage, n, n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage, stream);

@@ -114,6 +114,28 @@ def test_host_entry_point_matches_device_entry_point():
         api.ds4moe_destroy(h)
 
 
+def test_host_entry_point_pinned_decode_graph_matches_device_entry_point():
+    """Decode-sized forwards from page-locked host buffers run as one graph with the copies; the
+    result equals the device entry point bitwise, on repeat and with other buffers."""
+    import torch
+    p = synthetic.make_problem(SMALL_MIX)
+    h = moe_gpu.create(p)
+    try:
+        n, nh = 6, 2
+        xb = np.ascontiguousarray(p.x_bits[:n])
+        dev, _, _ = moe_gpu.forward(h, p, x_bits=xb, n_hash=nh)
+        for _ in range(2):  # two sets of buffers, each used twice (capture, then replay)
+            x_h = torch.from_numpy(xb.view(np.int16)).pin_memory()
+            t_h = torch.from_numpy(np.ascontiguousarray(p.token_ids[:nh], dtype=np.int32)).pin_memory()
+            o_h = torch.empty((n, SMALL_MIX.d), dtype=torch.float32).pin_memory()
+            for _ in range(2):
+                o_h.zero_()
+                api.ds4moe_forward_host(h, x_h.data_ptr(), n, t_h.data_ptr(), nh, o_h.data_ptr(), 0)
+                assert np.array_equal(o_h.numpy().view(np.uint32), dev.view(np.uint32))
+    finally:
+        api.ds4moe_destroy(h)
+
+
 def test_table_entries_outside_the_expert_range_are_refused():
     p = synthetic.make_problem(SMALL_MIX)
     bad = p.hash_table.copy()
