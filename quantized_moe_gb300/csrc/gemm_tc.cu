@@ -14,10 +14,10 @@
 //   warp 1     allocates TMEM; one thread issues the tcgen05.mma of every stage;
 //   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
 //              64-wide K stage;
-//   warps 3-18 dequantize: two warps per 16-row group, each turning half of the group's 64-wide
-//              K stage into fp16 weights in registers (exact small-integer quants, one fp16 FMA
-//              with the sub-block scale and min) and writing them with stmatrix straight into the
-//              swizzled A tile;
+//   warps 3-18 dequantize, in two groups of eight that take alternate K stages: each warp turns
+//              its 16-row group's 64-wide K stage into fp16 weights in registers (exact
+//              small-integer quants, one fp16 FMA with the sub-block scale and min) and writes
+//              them with stmatrix straight into the swizzled A tile;
 //   warps 19-22 epilogue: read the accumulator from TMEM (tcgen05.ld), one warp per lane
 //              quadrant, and release its buffer to the MMA.
 // Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) {
-      mbar_init(&b.a_full[i], kDeqWarps);
+      mbar_init(&b.a_full[i], kDeqWarps / 2);  // one group of dequant warps writes a stage
       mbar_init(&b.a_empty[i], 1);
     }
     for (int i = 0; i < B_STAGES; ++i) {
@@ -342,32 +342,40 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     }
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
+    // Two groups of eight warps take alternate K stages (the stage count per item is even); in a
+    // stage, warp rgw of the group turns all four 16-k sub-blocks of its 16-row group into fp16, so
+    // each warp has two independent halves of work and two stages are in progress at once.
     const int dw = warp - kFirstDeq;
-    const int rgw = dw & 7, half = dw >> 3;  // 16-row group of the slice, half of each K stage
-    // this lane's stmatrix row offsets for the warp's two sub-blocks of a stage (fixed per warp)
-    const uint32_t aoff[2] = {a_row_addr(0, rgw, 2 * half), a_row_addr(0, rgw, 2 * half + 1)};
-    Q2kRowConst rc{};  // constants of the current unit (Q2_K), refreshed when a unit starts
+    const int rgw = dw & 7, grp = dw >> 3;
+    // this lane's stmatrix row offsets for the four sub-blocks of a stage (fixed per warp)
+    const uint32_t aoff0[2] = {a_row_addr(0, rgw, 0), a_row_addr(0, rgw, 1)};
+    const uint32_t aoff1[2] = {a_row_addr(0, rgw, 2), a_row_addr(0, rgw, 3)};
+    Q2kRowConst rc{};  // constants of the current unit (Q2_K), refreshed at the group's first stage of it
     uint32_t gs = 0;
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
       for (int s = 0; s < n_stages; ++s, ++gs) {
+        if ((int)(gs & 1) != grp) continue;
         // the raw units follow the stages: unit gs / kpu of the CTA's sequence
         const uint32_t gu = gs / kpu;
         const int rs = gu % RAWS, sa = gs % A_STAGES, su = gs % kpu;
-        if (su == 0 && !mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
+        if (su == grp && !mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
         if (!mbar_wait(&b.a_empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
         if (FMT == FMT_Q2_K) {
-          if (su == 0) rc = q2k_row_const(unit);
-          deq_q2k(unit, su, a_base, half, aoff, rc);
-        } else
-          deq_q80(unit, su, a_base, half, aoff);
+          if (su == grp) rc = q2k_row_const(unit);
+          deq_q2k(unit, su, a_base, 0, aoff0, rc);
+          deq_q2k(unit, su, a_base, 1, aoff1, rc);
+        } else {
+          deq_q80(unit, su, a_base, 0, aoff0);
+          deq_q80(unit, su, a_base, 1, aoff1);
+        }
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&b.a_full[sa]);
-          if (su == kpu - 1) mbar_arrive(&b.raw_empty[rs]);
+          if (su == kpu - 2 + grp) mbar_arrive(&b.raw_empty[rs]);  // this warp's last stage of the unit
         }
       }
       if (!ok) break;
