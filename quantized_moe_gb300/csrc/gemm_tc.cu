@@ -87,32 +87,6 @@ __device__ __forceinline__ uint32_t a_row_addr(uint32_t a_base, int rg16, int sb
   return a_base + (row >> 3) * 1024 + (row & 7) * 128 + ((kc ^ (row & 7)) << 4);
 }
 
-// Two 16-k sub-blocks I0, I0 + 1 of a Q2_K chunk for this lane's rows g, g+8: every shift is a
-// constant (the field of sub-block 4 is already at mantissa bits 8-9).
-template <int I0>
-__device__ __forceinline__ void deq_q2k_pair(const uint32_t (&w)[4], uint32_t scw, __half2 d2, __half2 ndm2,
-                                             __half2 dm1024, uint32_t a_base, const uint32_t (&aoff)[2]) {
-  const __half2 k1024 = __float2half2_rn(1024.f);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    constexpr int kSh0 = 8 - 2 * I0;  // left shift of sub-block I0 (negative: right)
-    const int sh = kSh0 - 2 * j;
-    const uint32_t sc = scw >> (8 * j);
-    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), d2);  // 2^16 d s, rounded once
-    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), ndm2, dm1024);  // -dmin m
-    uint32_t a[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      // the quant pair moved to mantissa bits 8-9: the exact fp16 subnormal q * 2^-16, so one
-      // FMA with 2^16 d s gives d s q - dmin m with a single rounding
-      const uint32_t qb = (sh >= 0 ? (w[r] << sh) : (w[r] >> -sh)) & 0x03000300u;
-      a[r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
-                         : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
-    }
-    stmatrix_x4(a_base + aoff[j], a[0], a[1], a[2], a[3]);
-  }
-}
-
 // Per-row constants of a Q2_K unit for this lane's rows (g, g+8): 2^16 d (exact: only the exponent
 // changes; create refuses super-blocks whose 2^16 d * 15 would leave the fp16 range), -dmin and
 // 1024 dmin (m is read as the fp16 1024 + m, so one FMA gives -dmin * m rounded once).
@@ -132,82 +106,72 @@ __device__ __forceinline__ Q2kRowConst q2k_row_const(uint32_t unit) {
   return r;
 }
 
-// Dequantize half (32 k: two 16-k sub-blocks) of the 16 rows x 64 k of one Q2_K unit that fall in
-// K stage su (0..3) and store them.
-__device__ __forceinline__ void deq_q2k(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2],
-                                        const Q2kRowConst& rc) {
+// All four 16-k sub-blocks I0..I0+3 of a Q2_K stage for this lane's rows: every shared-memory load
+// first, then the arithmetic of the four sub-blocks (independent: it interleaves), then the four
+// stores.
+template <int I0>
+__device__ __forceinline__ void deq_q2k_quad(const uint32_t (&w)[4], uint32_t sc01, uint32_t sc23,
+                                             const Q2kRowConst& rc, uint32_t a_base, const uint32_t (&aoff)[4]) {
+  const __half2 k1024 = __float2half2_rn(1024.f);
+  uint32_t a[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int sh = 8 - 2 * (I0 + j);  // left shift of sub-block I0 + j's field (negative: right)
+    const uint32_t sc = (j < 2 ? sc01 : sc23) >> (8 * (j & 1));
+    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), rc.d2);
+    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), rc.ndm2, rc.dm1024);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t qb = (sh >= 0 ? (w[r] << sh) : (w[r] >> -sh)) & 0x03000300u;
+      a[j][r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
+                            : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) stmatrix_x4(a_base + aoff[j], a[j][0], a[j][1], a[j][2], a[j][3]);
+}
+
+// The 16 rows x 64 k of one Q2_K unit that fall in K stage su (0..3).
+__device__ __forceinline__ void deq_q2k_stage(uint32_t unit, int su, uint32_t a_base, const uint32_t (&aoff)[4],
+                                              const Q2kRowConst& rc) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
-  const int c = su >> 1, i0 = (su & 1) * 4 + 2 * half;  // first sub-block of the chunk handled here
+  const int c = su >> 1, i0 = (su & 1) * 4;
   const uint4 qw = lds128(unit + c * 512 + 16 * lane);
   const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
-  // scale bytes of sub-blocks i0, i0 + 1: byte 0/1 row g, byte 2/3 row g + 8
-  const uint32_t scw = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
-  switch (i0) {  // uniform across the warp
-    case 0: deq_q2k_pair<0>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
-    case 2: deq_q2k_pair<2>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
-    case 4: deq_q2k_pair<4>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
-    default: deq_q2k_pair<6>(w, scw, rc.d2, rc.ndm2, rc.dm1024, a_base, aoff); break;
-  }
+  const uint32_t sc01 = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
+  const uint32_t sc23 = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  if (i0 == 0)
+    deq_q2k_quad<0>(w, sc01, sc23, rc, a_base, aoff);
+  else
+    deq_q2k_quad<4>(w, sc01, sc23, rc, a_base, aoff);
 }
 
-// Dequantize half (two 16-k sub-blocks) of the 16 rows x 64 k of one Q8_0 unit (128 k) that fall
-// in K stage su (0..1).
-__device__ __forceinline__ void deq_q80(uint32_t unit, int su, uint32_t a_base, int half, const uint32_t (&aoff)[2]) {
+// The 16 rows x 64 k of one Q8_0 unit (128 k) that fall in K stage su (0..1): loads first, then
+// the four sub-blocks, then the stores.
+__device__ __forceinline__ void deq_q80_stage(uint32_t unit, int su, uint32_t a_base, const uint32_t (&aoff)[4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const __half2 k1152 = __float2half2_rn(1152.f);
+  uint4 v[2];
+  uint32_t scw[2];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int ii = 2 * half + j;  // sub-block of the stage
-    const int i = 4 * su + ii;    // MMA index (16-k sub-block) inside the unit
-    const uint4 v = lds128(unit + 512 * (i >> 1) + 16 * lane);
-    const uint32_t wa = (i & 1) ? v.z : v.x, wb = (i & 1) ? v.w : v.y;
-    const __half2 sc = u2h(lds32(unit + kQ80ScOff + 4 * (4 * g + (i >> 1))));  // block i/2: (row g, row g+8)
+  for (int h = 0; h < 2; ++h) {  // 32-weight block 2 su + h: sub-blocks 2h, 2h + 1 of the stage
+    v[h] = lds128(unit + 512 * (2 * su + h) + 16 * lane);
+    scw[h] = lds32(unit + kQ80ScOff + 4 * (4 * g + 2 * su + h));
+  }
+  uint32_t a[4][4];
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const uint4 vv = v[ii >> 1];
+    const uint32_t wa = (ii & 1) ? vv.z : vv.x, wb = (ii & 1) ? vv.w : vv.y;
+    const __half2 sc = u2h(scw[ii >> 1]);  // (row g, row g+8)
     const uint32_t raw[4] = {prmt(wa, 0x64u, 0x4140u), prmt(wa, 0x64u, 0x4342u), prmt(wb, 0x64u, 0x4140u),
                              prmt(wb, 0x64u, 0x4342u)};  // fp16 1024 + u, u = q + 128
-    uint32_t a[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
-      a[r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? __high2half2(sc) : __low2half2(sc)));
-    stmatrix_x4(a_base + aoff[j], a[0], a[1], a[2], a[3]);
+      a[ii][r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? __high2half2(sc) : __low2half2(sc)));
   }
-}
-
-// Waits (bounded, without raising errors) for a phase: used only to let copies land before exit.
-__device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try(bar, parity) && clock64() - t0 < kTimeoutCycles) {
-  }
-}
-
-// The tile of work item `it` (token tile, 128-row slice of the weights).
-struct Item {
-  int expert, row0, rows, nbox, n, mt;
-};
-
-__device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
-  Item t;
-  const int tile = it / p.m_tiles;
-  t.mt = it - tile * p.m_tiles;
-  if (p.tiles) {
-    const int4 v = __ldg(p.tiles + tile);
-    t.expert = v.x;
-    t.row0 = v.y;
-    t.rows = v.z;
-  } else {
-    t.expert = -1;
-    t.row0 = tile * BN;
-    t.rows = min(BN, p.n_rows - t.row0);
-  }
-  t.nbox = (max(t.rows, 1) + BOX_ROWS - 1) / BOX_ROWS;
-  t.n = t.nbox * BOX_ROWS;
-  return t;
-}
-
-// Work items of the launch: (token tiles) x (128-row slices of the weights), slices fastest so that
-// the CTAs running at the same time share their activation tiles through L2.
-__device__ __forceinline__ int item_count(const GemmArgs& p) {
-  const int tiles = p.tiles ? *p.n_tiles : (p.n_rows + BN - 1) / BN;
-  return tiles * p.m_tiles;
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) stmatrix_x4(a_base + aoff[ii], a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
 }
 
 template <int FMT, bool GATEUP>
@@ -348,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     const int dw = warp - kFirstDeq;
     const int rgw = dw & 7, grp = dw >> 3;
     // this lane's stmatrix row offsets for the four sub-blocks of a stage (fixed per warp)
-    const uint32_t aoff0[2] = {a_row_addr(0, rgw, 0), a_row_addr(0, rgw, 1)};
-    const uint32_t aoff1[2] = {a_row_addr(0, rgw, 2), a_row_addr(0, rgw, 3)};
+    const uint32_t aoff[4] = {a_row_addr(0, rgw, 0), a_row_addr(0, rgw, 1), a_row_addr(0, rgw, 2),
+                              a_row_addr(0, rgw, 3)};
     Q2kRowConst rc{};  // constants of the current unit (Q2_K), refreshed at the group's first stage of it
     uint32_t gs = 0;
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
@@ -365,11 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
         if (FMT == FMT_Q2_K) {
           if (su == grp) rc = q2k_row_const(unit);
-          deq_q2k(unit, su, a_base, 0, aoff0, rc);
-          deq_q2k(unit, su, a_base, 1, aoff1, rc);
+          deq_q2k_stage(unit, su, a_base, aoff, rc);
         } else {
-          deq_q80(unit, su, a_base, 0, aoff0);
-          deq_q80(unit, su, a_base, 1, aoff1);
+          deq_q80_stage(unit, su, a_base, aoff);
         }
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
