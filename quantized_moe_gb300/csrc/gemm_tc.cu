@@ -146,6 +146,44 @@ __device__ __forceinline__ void deq_q2k_stage(uint32_t unit, int su, uint32_t a_
     deq_q2k_quad<4>(w, sc01, sc23, rc, a_base, aoff);
 }
 
+// Waits (bounded, without raising errors) for a phase: used only to let copies land before exit.
+__device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity) && clock64() - t0 < kTimeoutCycles) {
+  }
+}
+
+// The tile of work item `it` (token tile, 128-row slice of the weights).
+struct Item {
+  int expert, row0, rows, nbox, n, mt;
+};
+
+__device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
+  Item t;
+  const int tile = it / p.m_tiles;
+  t.mt = it - tile * p.m_tiles;
+  if (p.tiles) {
+    const int4 v = __ldg(p.tiles + tile);
+    t.expert = v.x;
+    t.row0 = v.y;
+    t.rows = v.z;
+  } else {
+    t.expert = -1;
+    t.row0 = tile * BN;
+    t.rows = min(BN, p.n_rows - t.row0);
+  }
+  t.nbox = (max(t.rows, 1) + BOX_ROWS - 1) / BOX_ROWS;
+  t.n = t.nbox * BOX_ROWS;
+  return t;
+}
+
+// Work items of the launch: (token tiles) x (128-row slices of the weights), slices fastest so that
+// the CTAs running at the same time share their activation tiles through L2.
+__device__ __forceinline__ int item_count(const GemmArgs& p) {
+  const int tiles = p.tiles ? *p.n_tiles : (p.n_rows + BN - 1) / BN;
+  return tiles * p.m_tiles;
+}
+
 // The 16 rows x 64 k of one Q8_0 unit (128 k) that fall in K stage su (0..1): loads first, then
 // the four sub-blocks, then the stores.
 __device__ __forceinline__ void deq_q80_stage(uint32_t unit, int su, uint32_t a_base, const uint32_t (&aoff)[4]) {
