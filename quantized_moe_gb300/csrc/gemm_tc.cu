@@ -75,6 +75,10 @@ struct Bars {
   uint64_t* acc_empty;  // [2] epilogue -> MMA
 };
 
+// silu(g) * u with the hardware exponential and division (a few ulp, far inside the tolerance):
+// the epilogue shares issue slots with the dequant warps.
+__device__ __forceinline__ float silu_mul_fast(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
+
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
               if (col < t.rows) {
-                const float h = silu_mul(gbuf[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
+                const float h = silu_mul_fast(gbuf[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
                 bad |= !(fabsf(h) <= 65504.f);
                 p.h_out[(size_t)(t.row0 + col) * p.ld_out + feat] = __float2half_rn(h);
               }
