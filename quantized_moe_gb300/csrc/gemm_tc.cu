@@ -34,8 +34,6 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_STAGES = 3;  // dequantized weight tiles
-constexpr int B_STAGES = 3;  // activation tiles (TMA from L2/HBM)
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
@@ -48,15 +46,20 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;  // double-buffered: the epilogue of one
 
 // Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
 // Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
+#ifndef GEMM_Q2K_STAGES
+#define GEMM_Q2K_STAGES 3
+#endif
 template <int FMT>
 struct Cfg {
   static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);
   static constexpr int RAWS = FMT == FMT_Q2_K ? 4 : 3;
+  // K stages in flight: each holds a dequantized weight tile (A) and an activation tile (B)
+  static constexpr int STAGES = FMT == FMT_Q2_K ? GEMM_Q2K_STAGES : 3;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + A_STAGES * A_BYTES;
-  static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
-  static constexpr int N_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * RAWS + 4;
+  static constexpr int N_BARS = 2 * STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
   static constexpr int GBUF_BYTES = 64 * 16 * 4;  // 16 columns x 64 gate rows fp32 (epilogue exchange)
@@ -64,11 +67,11 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+// One full/empty pair per K stage for both operands: the MMA thread makes one wait and one commit
+// per stage, and the dequant warps and the activation producer wait on the same release.
 struct Bars {
-  uint64_t* a_full;     // [A_STAGES] dequant warps -> MMA
-  uint64_t* a_empty;    // [A_STAGES] MMA commit -> dequant
-  uint64_t* b_full;     // [B_STAGES] activation TMA -> MMA
-  uint64_t* b_empty;    // [B_STAGES] MMA commit -> producer
+  uint64_t* full;       // [STAGES] dequant group (A) + activation TMA (B, with its bytes) -> MMA
+  uint64_t* empty;      // [STAGES] MMA commit -> dequant group and activation producer
   uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
   uint64_t* raw_empty;  // [RAWS] dequant -> producer
   uint64_t* acc_full;   // [2] MMA -> epilogue
@@ -157,7 +160,16 @@ __device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// The tile of work item `it` (token tile, 128-row slice of the weights).
+// mbar_wait by lane 0 of a converged warp, its result given to every lane.
+__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err, site);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// The tile of work item `it` (token tile, 128-row slice of the weights): `nbox` activation boxes
+// of 64 rows are loaded, and the MMA's N (the accumulator columns the epilogue reads) is the row
+// count rounded up to the instruction's granularity of 16, not to the box.
 struct Item {
   int expert, row0, rows, nbox, n, mt;
 };
@@ -177,7 +189,7 @@ __device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
     t.rows = min(BN, p.n_rows - t.row0);
   }
   t.nbox = (max(t.rows, 1) + BOX_ROWS - 1) / BOX_ROWS;
-  t.n = t.nbox * BOX_ROWS;
+  t.n = (max(t.rows, 1) + 15) / 16 * 16;
   return t;
 }
 
@@ -224,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
+  constexpr int STAGES = C::STAGES;
   const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
   const int n_items = item_count(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
@@ -231,11 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
   Bars b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  b.a_full = bars;
-  b.a_empty = bars + A_STAGES;
-  b.b_full = bars + 2 * A_STAGES;
-  b.b_empty = bars + 2 * A_STAGES + B_STAGES;
-  b.raw_full = bars + 2 * A_STAGES + 2 * B_STAGES;
+  b.full = bars;
+  b.empty = bars + STAGES;
+  b.raw_full = bars + 2 * STAGES;
   b.raw_empty = b.raw_full + RAWS;
   b.acc_full = b.raw_empty + RAWS;   // [2]
   b.acc_empty = b.acc_full + 2;      // [2]
@@ -244,13 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   float* gbuf = reinterpret_cast<float*>(smem + C::OFF_GBUF);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < A_STAGES; ++i) {
-      mbar_init(&b.a_full[i], kDeqWarps / 2);  // one group of dequant warps writes a stage
-      mbar_init(&b.a_empty[i], 1);
-    }
-    for (int i = 0; i < B_STAGES; ++i) {
-      mbar_init(&b.b_full[i], 1);
-      mbar_init(&b.b_empty[i], 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&b.full[i], kDeqWarps / 2 + 1);  // one group of dequant warps + the activation producer
+      mbar_init(&b.empty[i], 1);
     }
     for (int r = 0; r < RAWS; ++r) {
       mbar_init(&b.raw_full[r], 1);
@@ -301,50 +308,47 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
         const Item t = item_of(p, it);
         for (int sB = 0; sB < n_stages; ++sB, ++gs) {
-          const int sb = gs % B_STAGES;
-          if (!mbar_wait(&b.b_empty[sb], ((gs / B_STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
+          const int sb = gs % STAGES;
+          if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * B_BYTES;
-          mbar_expect_tx(&b.b_full[sb], t.nbox * BOX_ROWS * BK * 2);
+          mbar_expect_tx(&b.full[sb], t.nbox * BOX_ROWS * BK * 2);
           for (int bx = 0; bx < t.nbox; ++bx)
-            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, t.row0 + bx * BOX_ROWS, &b.b_full[sb]);
+            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, t.row0 + bx * BOX_ROWS, &b.full[sb]);
         }
       }
-      for (uint32_t k = gs > (uint32_t)B_STAGES ? gs - B_STAGES : 0; k < gs; ++k)
-        bounded_try(&b.b_full[k % B_STAGES], (k / B_STAGES) & 1);
+      for (uint32_t k = gs > (uint32_t)STAGES ? gs - STAGES : 0; k < gs; ++k)
+        bounded_try(&b.full[k % STAGES], (k / STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t gs = 0;
-      int local = 0;  // items of this CTA so far: accumulator buffer local & 1
-      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++local) {
-        const Item t = item_of(p, it);
-        const int buf = local & 1;
-        // the epilogue has drained this buffer (item local - 2)
-        if (!mbar_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6)) break;
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16_f32(BM, t.n);
-        const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS);
-        bool ok = true;
-        for (int s = 0; s < n_stages; ++s, ++gs) {
-          const int sa = gs % A_STAGES, sb = gs % B_STAGES;
-          if (!mbar_wait(&b.a_full[sa], (gs / A_STAGES) & 1, abort_flag, p.err, 7) ||
-              !mbar_wait(&b.b_full[sb], (gs / B_STAGES) & 1, abort_flag, p.err, 8)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + sa * A_BYTES));
-          const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + sb * B_BYTES));
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
-            tc_mma_f16(acc, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-          tc_commit(&b.a_empty[sa]);
-          tc_commit(&b.b_empty[sb]);
+    // The whole warp runs the loop; lane 0 polls the barriers and one elected lane issues.
+    uint32_t gs = 0;
+    int local = 0;  // items of this CTA so far: accumulator buffer local & 1
+    for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++local) {
+      const Item t = item_of(p, it);
+      const int buf = local & 1;
+      // the epilogue has drained this buffer (item local - 2)
+      if (!lane0_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6)) break;
+      tc_fence_after();
+      const uint32_t idesc = idesc_f16_f32(BM, t.n);
+      const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS);
+      bool ok = true;
+      for (int s = 0; s < n_stages; ++s, ++gs) {
+        const int st = gs % STAGES;
+        if (!lane0_wait(&b.full[st], (gs / STAGES) & 1, abort_flag, p.err, 7)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc_commit(&b.acc_full[buf]);
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + st * A_BYTES));
+        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + st * B_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
+          tc_mma_f16_elect(acc, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+        tc_commit_elect(&b.empty[st]);
       }
+      if (!ok) break;
+      tc_commit_elect(&b.acc_full[buf]);
     }
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
@@ -364,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         if ((int)(gs & 1) != grp) continue;
         // the raw units follow the stages: unit gs / kpu of the CTA's sequence
         const uint32_t gu = gs / kpu;
-        const int rs = gu % RAWS, sa = gs % A_STAGES, su = gs % kpu;
+        const int rs = gu % RAWS, sa = gs % STAGES, su = gs % kpu;
         if (su == grp && !mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
-        if (!mbar_wait(&b.a_empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
+        if (!mbar_wait(&b.empty[sa], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
         if (FMT == FMT_Q2_K) {
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&b.a_full[sa]);
+          mbar_arrive(&b.full[sa]);
           if (su == kpu - 2 + grp) mbar_arrive(&b.raw_empty[rs]);  // this warp's last stage of the unit
         }
       }
