@@ -194,7 +194,8 @@ struct GemmArgs {
   int* err;                // error bits: 4 = a pipeline wait timed out, 8 = |h| beyond fp16 range
 };
 
-int gemm_tile_n();
+// Largest token tile the expert GEMM takes for a weight format (FMT_*).
+int gemm_tile_n(int fmt);
 cudaError_t gemm_prepare();
 cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& p, int m_tiles, int n_tiles,
                         cudaStream_t s);

@@ -264,6 +264,12 @@ namespace {
 
 bool fmt_ok(int f) { return f == DS4MOE_FMT_Q8_0 || f == DS4MOE_FMT_Q2_K; }
 
+// Token tile of the routed expert GEMMs: the gate/up and the down GEMM share one tiling, so it is
+// the smaller of the two formats' tiles.
+int routed_tile_n(const ds4moe_shapes& s) {
+  return std::min(ds4::gemm_tile_n(s.fmt_gate_up), ds4::gemm_tile_n(s.fmt_down));
+}
+
 int check_shapes(const ds4moe_shapes* s) {
   // the router stages 8 token rows of d bf16 values in shared memory: d <= 12288 keeps that under 200 KB
   if (s->d <= 0 || s->d % 128 || s->d > 12288) return fail(DS4MOE_ERR_INVALID_ARG, "d=%d must be a positive multiple of 128 up to 12288", s->d);
@@ -480,7 +486,8 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
     DS4_TRY(h->alloc_t(&h->H16, slots * f * 2));
     DS4_TRY(h->alloc_t(&h->inv_s, M * 4));
     DS4_TRY(h->alloc_t(&h->inv_p, slots * 4));
-    const size_t max_tiles = (slots + ds4::gemm_tile_n() - 1) / ds4::gemm_tile_n() + E;
+    const int tn = routed_tile_n(*s);
+    const size_t max_tiles = (slots + tn - 1) / tn + E;
     DS4_TRY(h->alloc_t(&h->tiles, max_tiles * sizeof(int4)));
     DS4_TRY(h->alloc_t(&h->n_tiles, 4));
     if (s->n_shared) {
@@ -640,9 +647,9 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   mark("xprep");
   ds4::launch_gather(h->Xs16, h->inv_s, h->perm, n * K, K, d, h->Xp16, h->inv_p, st);
   mark("gather");
-  ds4::launch_tiles(h->counts, h->offsets, E, ds4::gemm_tile_n(), h->tiles, h->n_tiles, st);
+  const int TN = routed_tile_n(s);  // one tiling serves the gate/up and the down GEMM
+  ds4::launch_tiles(h->counts, h->offsets, E, TN, h->tiles, h->n_tiles, st);
   mark("tiles");
-  const int TN = ds4::gemm_tile_n();
   const int routed_tiles = (n * K + TN - 1) / TN + std::min(E, n * K), dense_tiles = (n + TN - 1) / TN;
   ds4::GemmArgs g{};
   g.w0 = h->gate; g.w1 = h->up; g.mat_bytes = h->mb_gu; g.k = d; g.tiles = h->tiles; g.n_tiles = h->n_tiles;

@@ -33,31 +33,38 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
 constexpr int kDeqWarps = 16;
 constexpr int kFirstDeq = 3;  // warps 0-2: weight producer, MMA, activation producer
 constexpr int kEpiWarps = 4;  // warps 19-22: epilogue, one per TMEM lane quadrant
 constexpr int kThreads = (kFirstDeq + kDeqWarps + kEpiWarps) * 32;  // 736
-constexpr int ACC_COLS = 256;            // one fp32 accumulator of 128 x BN
+constexpr int ACC_COLS = 256;            // TMEM columns per accumulator (128 x N fp32, N <= 256)
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // double-buffered: the epilogue of one item overlaps the next
 
 // Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
 // Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
 #ifndef GEMM_Q2K_STAGES
-#define GEMM_Q2K_STAGES 3
+#define GEMM_Q2K_STAGES 4
+#endif
+#ifndef GEMM_Q2K_BN
+#define GEMM_Q2K_BN 192
 #endif
 template <int FMT>
 struct Cfg {
   static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);
   static constexpr int RAWS = FMT == FMT_Q2_K ? 4 : 3;
+  // Token tile (MMA N at most): Q2_K takes 192 tokens so that four K stages fit in shared memory,
+  // Q8_0 (larger raw units) 256 with three.
+  static constexpr int BN = FMT == FMT_Q2_K ? GEMM_Q2K_BN : 256;
+  static constexpr int B_BYTES = BN * BK * 2;
   // K stages in flight: each holds a dequantized weight tile (A) and an activation tile (B)
   static constexpr int STAGES = FMT == FMT_Q2_K ? GEMM_Q2K_STAGES : 3;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
+  static_assert(BN % BOX_ROWS == 0 && BN <= ACC_COLS, "token tile");
   static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
   static constexpr int N_BARS = 2 * STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
@@ -174,6 +181,7 @@ struct Item {
   int expert, row0, rows, nbox, n, mt;
 };
 
+template <int BN>
 __device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
   Item t;
   const int tile = it / p.m_tiles;
@@ -195,6 +203,7 @@ __device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
 
 // Work items of the launch: (token tiles) x (128-row slices of the weights), slices fastest so that
 // the CTAs running at the same time share their activation tiles through L2.
+template <int BN>
 __device__ __forceinline__ int item_count(const GemmArgs& p) {
   const int tiles = p.tiles ? *p.n_tiles : (p.n_rows + BN - 1) / BN;
   return tiles * p.m_tiles;
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
   constexpr int STAGES = C::STAGES;
   const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
-  const int n_items = item_count(p);
+  const int n_items = item_count<C::BN>(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
   const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
 
@@ -284,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     if (lane == 0) {
       uint32_t gu = 0;  // K units issued by this CTA over all its items
       for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
-        const Item t = item_of(p, it);
+        const Item t = item_of<C::BN>(p, it);
         const size_t eoff = t.expert >= 0 ? (size_t)t.expert * p.mat_bytes : 0;
         const uint8_t* src0 = p.w0 + eoff;
         const uint8_t* src1 = GATEUP ? p.w1 + eoff : nullptr;
@@ -306,11 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     if (lane == 0) {
       uint32_t gs = 0;  // stages issued over all items
       for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
-        const Item t = item_of(p, it);
+        const Item t = item_of<C::BN>(p, it);
         for (int sB = 0; sB < n_stages; ++sB, ++gs) {
           const int sb = gs % STAGES;
           if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
-          unsigned char* bdst = smem + C::OFF_B + sb * B_BYTES;
+          unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
           mbar_expect_tx(&b.full[sb], t.nbox * BOX_ROWS * BK * 2);
           for (int bx = 0; bx < t.nbox; ++bx)
             tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, t.row0 + bx * BOX_ROWS, &b.full[sb]);
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     uint32_t gs = 0;
     int local = 0;  // items of this CTA so far: accumulator buffer local & 1
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++local) {
-      const Item t = item_of(p, it);
+      const Item t = item_of<C::BN>(p, it);
       const int buf = local & 1;
       // the epilogue has drained this buffer (item local - 2)
       if (!lane0_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6)) break;
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
         tc_fence_after();
         const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + st * A_BYTES));
-        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + st * B_BYTES));
+        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + st * C::B_BYTES));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
           tc_mma_f16_elect(acc, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     const int row = 32 * quad + lane;     // slice row = TMEM lane
     int local = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-      const Item t = item_of(p, it);
+      const Item t = item_of<C::BN>(p, it);
       const int buf = local & 1;
       // all four warps enter the item's epilogue (it has named barriers) only together
       if (!named_bar_all(1, 32 * kEpiWarps, mbar_wait(&b.acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 5)))
@@ -462,7 +471,7 @@ cudaError_t prepare_one() {
 
 }  // namespace
 
-int gemm_tile_n() { return BN; }
+int gemm_tile_n(int fmt) { return fmt == FMT_Q2_K ? Cfg<FMT_Q2_K>::BN : Cfg<FMT_Q8_0>::BN; }
 
 cudaError_t gemm_prepare() {
   cudaError_t e = prepare_one<FMT_Q2_K, true>();
