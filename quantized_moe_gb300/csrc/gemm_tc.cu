@@ -1,23 +1,28 @@
 // Prefill expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
-// Persistent: one CTA per SM loops over work items, each a 128-row x N-token tile (N <= 256, a
-// multiple of 64) of one expert:
+// Persistent: one CTA per SM loops over work items, each a 128-row x N-token tile of one expert
+// (N <= 192 tokens for Q2_K weights, <= 256 for Q8_0; the MMA's N is the token count rounded up
+// to 16):
 //   gate/up: the 128 rows interleave 64 gate rows and the 64 up rows of the same features, so
 //            the epilogue forms h = silu(g) * u for 64 features and writes it as fp16;
 //   down:    128 rows of d, written as fp32 per bucketed slot for the fixed-order combine.
 // The weight, activation and dequantized-tile pipelines run on across items, and the fp32
 // accumulator is double-buffered in TMEM (2 x 256 columns), so the epilogue of one item overlaps
-// the main loop of the next.
-// Warp roles (19 warps):
+// the main loop of the next. Each K stage (64 wide) has one full barrier, completed by the
+// dequant group that wrote its A tile and by the activation TMA, and one empty barrier, completed
+// by the MMA commit.
+// Warp roles (23 warps):
 //   warp 0     weight producer: bulk-copies the packed weight units of each K unit (256 k for
 //              Q2_K, 128 k for Q8_0) of the tile's rows;
-//   warp 1     allocates TMEM; one thread issues the tcgen05.mma of every stage;
+//   warp 1     allocates TMEM; the converged warp runs the MMA loop and one elected lane issues
+//              the tcgen05.mma and commits of every stage;
 //   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
-//              64-wide K stage;
-//   warps 3-18 dequantize, in two groups of eight that take alternate K stages: each warp turns
-//              its 16-row group's 64-wide K stage into fp16 weights in registers (exact
-//              small-integer quants, one fp16 FMA with the sub-block scale and min) and writes
-//              them with stmatrix straight into the swizzled A tile;
+//              K stage;
+//   warps 3-18 dequantize, in one group per K stage of a raw unit (four groups of four warps for
+//              Q2_K, two of eight for Q8_0) taking the stages round-robin: each warp turns its
+//              16-row groups' 64-wide K stage into fp16 weights in registers (exact small-integer
+//              quants, one fp16 FMA with the sub-block scale and min) and writes them with
+//              stmatrix straight into the swizzled A tile;
 //   warps 19-22 epilogue: read the accumulator from TMEM (tcgen05.ld), one warp per lane
 //              quadrant, and release its buffer to the MMA.
 // Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
@@ -69,7 +74,9 @@ struct Cfg {
   static constexpr int N_BARS = 2 * STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
-  static constexpr int GBUF_BYTES = 64 * 16 * 4;  // 16 columns x 64 gate rows fp32 (epilogue exchange)
+  // gate/up epilogue: two parities x (8 columns of g + 8 columns of u) x 64 features fp32, then the
+  // 1 / scale of each token of the tile
+  static constexpr int GBUF_BYTES = 2 * 2 * 8 * 64 * 4 + 256 * 4;
   static constexpr int SMEM_BYTES = OFF_GBUF + GBUF_BYTES + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -120,44 +127,58 @@ __device__ __forceinline__ Q2kRowConst q2k_row_const(uint32_t unit) {
   return r;
 }
 
-// All four 16-k sub-blocks I0..I0+3 of a Q2_K stage for this lane's rows: every shared-memory load
-// first, then the arithmetic of the four sub-blocks (independent: it interleaves), then the four
-// stores.
-template <int I0>
-__device__ __forceinline__ void deq_q2k_quad(const uint32_t (&w)[4], uint32_t sc01, uint32_t sc23,
-                                             const Q2kRowConst& rc, uint32_t a_base, const uint32_t (&aoff)[4]) {
+// All four 16-k sub-blocks I0..I0+3 of a Q2_K stage for this lane's rows in each of the warp's NR
+// 16-row groups: the arithmetic of every (group, sub-block) pair is independent and interleaves,
+// then the stores follow.
+template <int I0, int NR>
+__device__ __forceinline__ void deq_q2k_quad(const uint32_t (&w)[NR][4], const uint32_t (&sc01)[NR],
+                                             const uint32_t (&sc23)[NR], const Q2kRowConst (&rc)[NR],
+                                             uint32_t a_base, const uint32_t (&aoff)[NR][4]) {
   const __half2 k1024 = __float2half2_rn(1024.f);
-  uint32_t a[4][4];
+  uint32_t a[NR][4][4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int sh = 8 - 2 * (I0 + j);  // left shift of sub-block I0 + j's field (negative: right)
-    const uint32_t sc = (j < 2 ? sc01 : sc23) >> (8 * (j & 1));
-    const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), rc.d2);
-    const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), rc.ndm2, rc.dm1024);
+  for (int n = 0; n < NR; ++n) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t qb = (sh >= 0 ? (w[r] << sh) : (w[r] >> -sh)) & 0x03000300u;
-      a[j][r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
-                            : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
+    for (int j = 0; j < 4; ++j) {
+      const int sh = 8 - 2 * (I0 + j);  // left shift of sub-block I0 + j's field (negative: right)
+      const uint32_t sc = (j < 2 ? sc01[n] : sc23[n]) >> (8 * (j & 1));
+      const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), rc[n].d2);
+      const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), rc[n].ndm2, rc[n].dm1024);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t qb = (sh >= 0 ? (w[n][r] << sh) : (w[n][r] >> -sh)) & 0x03000300u;
+        a[n][j][r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
+                                 : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
+      }
     }
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) stmatrix_x4(a_base + aoff[j], a[j][0], a[j][1], a[j][2], a[j][3]);
+  for (int n = 0; n < NR; ++n)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) stmatrix_x4(a_base + aoff[n][j], a[n][j][0], a[n][j][1], a[n][j][2], a[n][j][3]);
 }
 
-// The 16 rows x 64 k of one Q2_K unit that fall in K stage su (0..3).
-__device__ __forceinline__ void deq_q2k_stage(uint32_t unit, int su, uint32_t a_base, const uint32_t (&aoff)[4],
-                                              const Q2kRowConst& rc) {
+// The 16 rows x 64 k of K stage su (0..3) of NR Q2_K units (one per 16-row group of the warp).
+template <int NR>
+__device__ __forceinline__ void deq_q2k_stage(const uint32_t (&unit)[NR], int su, uint32_t a_base,
+                                              const uint32_t (&aoff)[NR][4], const Q2kRowConst (&rc)[NR]) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const int c = su >> 1, i0 = (su & 1) * 4;
-  const uint4 qw = lds128(unit + c * 512 + 16 * lane);
-  const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
-  const uint32_t sc01 = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
-  const uint32_t sc23 = lds32(unit + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  uint32_t w[NR][4], sc01[NR], sc23[NR];
+#pragma unroll
+  for (int n = 0; n < NR; ++n) {
+    const uint4 qw = lds128(unit[n] + c * 512 + 16 * lane);
+    w[n][0] = qw.x;
+    w[n][1] = qw.y;
+    w[n][2] = qw.z;
+    w[n][3] = qw.w;
+    sc01[n] = lds32(unit[n] + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
+    sc23[n] = lds32(unit[n] + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  }
   if (i0 == 0)
-    deq_q2k_quad<0>(w, sc01, sc23, rc, a_base, aoff);
+    deq_q2k_quad<0, NR>(w, sc01, sc23, rc, a_base, aoff);
   else
-    deq_q2k_quad<4>(w, sc01, sc23, rc, a_base, aoff);
+    deq_q2k_quad<4, NR>(w, sc01, sc23, rc, a_base, aoff);
 }
 
 // Waits (bounded, without raising errors) for a phase: used only to let copies land before exit.
@@ -246,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
   constexpr int STAGES = C::STAGES;
+  // dequant groups (one per K stage of a raw unit), warps per group, 16-row groups per warp
+  constexpr int NG = UK / BK, WPG = kDeqWarps / NG, RPW = 8 / WPG;
+  static_assert(NG <= STAGES && WPG * RPW == 8, "dequant groups");
   const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
   const int n_items = item_count<C::BN>(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
@@ -262,10 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* gbuf = reinterpret_cast<float*>(smem + C::OFF_GBUF);
+  float* ibuf = gbuf + 2048;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&b.full[i], kDeqWarps / 2 + 1);  // one group of dequant warps + the activation producer
+      mbar_init(&b.full[i], WPG + 1);  // one group of dequant warps + the activation producer
       mbar_init(&b.empty[i], 1);
     }
     for (int r = 0; r < RAWS; ++r) {
@@ -361,38 +386,48 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     }
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
-    // Two groups of eight warps take alternate K stages (the stage count per item is even); in a
-    // stage, warp rgw of the group turns all four 16-k sub-blocks of its 16-row group into fp16, so
-    // each warp has two independent halves of work and two stages are in progress at once.
+    // NG groups of warps take K stages round-robin, NG = the stages per raw unit (Q2_K four, Q8_0
+    // two), so each group dequantizes one stage of every unit and NG stages are in progress at
+    // once. In a stage, each warp of a group turns all four 16-k sub-blocks of its RPW 16-row
+    // groups into fp16: 4 * RPW independent pieces of work per lane.
     const int dw = warp - kFirstDeq;
-    const int rgw = dw & 7, grp = dw >> 3;
-    // this lane's stmatrix row offsets for the four sub-blocks of a stage (fixed per warp)
-    const uint32_t aoff[4] = {a_row_addr(0, rgw, 0), a_row_addr(0, rgw, 1), a_row_addr(0, rgw, 2),
-                              a_row_addr(0, rgw, 3)};
-    Q2kRowConst rc{};  // constants of the current unit (Q2_K), refreshed at the group's first stage of it
+    const int grp = dw / WPG, wi = dw % WPG;
+    // this lane's stmatrix row offsets for the sub-blocks of a stage (fixed per warp)
+    uint32_t aoff[RPW][4];
+#pragma unroll
+    for (int n = 0; n < RPW; ++n)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) aoff[n][j] = a_row_addr(0, wi + WPG * n, j);
     uint32_t gs = 0;
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
       for (int s = 0; s < n_stages; ++s, ++gs) {
-        if ((int)(gs & 1) != grp) continue;
-        // the raw units follow the stages: unit gs / kpu of the CTA's sequence
+        if ((int)(gs % NG) != grp) continue;
+        // the raw units follow the stages: unit gs / kpu of the CTA's sequence (kpu == NG)
         const uint32_t gu = gs / kpu;
         const int rs = gu % RAWS, sa = gs % STAGES, su = gs % kpu;
-        if (su == grp && !mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
+        if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
         if (!mbar_wait(&b.empty[sa], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
-        const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES + rgw * UB);
+        const uint32_t raw = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
-        if (FMT == FMT_Q2_K) {
-          if (su == grp) rc = q2k_row_const(unit);
-          deq_q2k_stage(unit, su, a_base, aoff, rc);
+        if constexpr (FMT == FMT_Q2_K) {
+          uint32_t unit[RPW];
+          Q2kRowConst rc[RPW];
+#pragma unroll
+          for (int n = 0; n < RPW; ++n) {
+            unit[n] = raw + (wi + WPG * n) * UB;
+            rc[n] = q2k_row_const(unit[n]);
+          }
+          deq_q2k_stage<RPW>(unit, su, a_base, aoff, rc);
         } else {
-          deq_q80_stage(unit, su, a_base, aoff);
+#pragma unroll
+          for (int n = 0; n < RPW; ++n) deq_q80_stage(raw + (wi + WPG * n) * UB, su, a_base, aoff[n]);
         }
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&b.full[sa]);
-          if (su == kpu - 2 + grp) mbar_arrive(&b.raw_empty[rs]);  // this warp's last stage of the unit
+          mbar_arrive(&b.raw_empty[rs]);  // the group's only stage of this unit is done
         }
       }
       if (!ok) break;
@@ -409,35 +444,44 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       if (!named_bar_all(1, 32 * kEpiWarps, mbar_wait(&b.acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 5)))
         break;
       tc_fence_after();
+      if (GATEUP) {  // the tile's activation scales, once per item
+        for (int i = threadIdx.x - 32 * (kFirstDeq + kDeqWarps); i < t.n; i += 32 * kEpiWarps)
+          ibuf[i] = i < t.rows ? __ldg(p.inv_scale + t.row0 + i) : 0.f;
+        named_bar(1, 32 * kEpiWarps);
+      }
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC_COLS) + ((uint32_t)(32 * quad) << 16);
       for (int c0 = 0; c0 < t.n; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(taddr + c0, r);
         tmem_ld_wait();
         if (GATEUP) {
-          if (quad < 2) {  // gate rows: hand g to the up warps through shared memory
+          // The gate warps (TMEM lanes 0-63) form h for the chunk's first 8 columns, the up warps
+          // (lanes 64-127) for the last 8: each hands the other half of its accumulator rows over.
+          const int pb = (c0 >> 4) & 1, feat = row & 63;
+          float* xg = gbuf + pb * 1024;  // [8][64] g of columns c0+8 .. c0+15
+          float* xu = xg + 512;          // [8][64] u of columns c0 .. c0+7
+          const bool gate = quad < 2;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gbuf[j * 64 + row] = __uint_as_float(r[j]);
+          for (int j = 0; j < 8; ++j) {
+            if (gate) xg[j * 64 + feat] = __uint_as_float(r[8 + j]);
+            else xu[j * 64 + feat] = __uint_as_float(r[j]);
           }
           named_bar(1, 32 * kEpiWarps);
-          if (quad >= 2) {
-            const int feat = 64 * t.mt + row - 64;
-            float inv[16];
+          const int cb = c0 + (gate ? 0 : 8);
+          unsigned bad = 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) inv[j] = c0 + j < t.rows ? __ldg(p.inv_scale + t.row0 + c0 + j) : 0.f;
-            unsigned bad = 0;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < t.rows) {
-                const float h = silu_mul_fast(gbuf[j * 64 + row - 64] * inv[j], __uint_as_float(r[j]) * inv[j]);
-                bad |= !(fabsf(h) <= 65504.f);
-                p.h_out[(size_t)(t.row0 + col) * p.ld_out + feat] = __float2half_rn(h);
-              }
+          for (int j = 0; j < 8; ++j) {
+            const int col = cb + j;
+            if (col < t.rows) {
+              const float g = gate ? __uint_as_float(r[j]) : xg[j * 64 + feat];
+              const float u = gate ? xu[j * 64 + feat] : __uint_as_float(r[8 + j]);
+              const float iv = ibuf[col];
+              const float h = silu_mul_fast(g * iv, u * iv);
+              bad |= !(fabsf(h) <= 65504.f);
+              p.h_out[(size_t)(t.row0 + col) * p.ld_out + 64 * t.mt + feat] = __float2half_rn(h);
             }
-            if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 8);
           }
-          named_bar(1, 32 * kEpiWarps);
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 8);
         } else {
           const int drow = 128 * t.mt + row;
 #pragma unroll
