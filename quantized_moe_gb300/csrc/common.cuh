@@ -197,9 +197,14 @@ struct GemmArgs {
 // Largest token tile the expert GEMM takes for a weight format (FMT_*).
 int gemm_tile_n(int fmt);
 cudaError_t gemm_prepare();
-cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& p, int m_tiles, int n_tiles,
+// TMA maps of one row-major fp16 activation buffer: 64 columns x 64 rows and x 128 rows per box
+// (a tile's rows are fetched with as few boxes as the two sizes allow).
+struct ActMaps {
+  CUtensorMap r64, r128;
+};
+cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int m_tiles, int n_tiles,
                         cudaStream_t s);
-int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols);
+int make_act_maps(ActMaps* tm, const void* base, uint64_t rows, uint64_t cols);
 
 // Prefill preparation (see prefill_prep.cu).
 void launch_xprep(const __nv_bfloat16* x, int n_tok, int d, __half* xs16, float* inv_s, cudaStream_t s);

@@ -105,7 +105,7 @@ struct ds4moe_handle {
   int4* tiles = nullptr;
   int* n_tiles = nullptr;
   bool has_prefill = false;
-  CUtensorMap tm_xp, tm_xs, tm_h, tm_hs;
+  ds4::ActMaps tm_xp, tm_xs, tm_h, tm_hs;
   int* err = nullptr;
   float* xmax = nullptr;
   float* hmax = nullptr;
@@ -494,10 +494,10 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
       DS4_TRY(h->alloc_t(&h->Ys, M * d * 4));
       DS4_TRY(h->alloc_t(&h->Hs16, M * fs * 2));
     }
-    int tr = ds4::make_tmap_f16(&h->tm_xp, h->Xp16, slots, d);
-    if (!tr) tr = ds4::make_tmap_f16(&h->tm_xs, h->Xs16, M, d);
-    if (!tr) tr = ds4::make_tmap_f16(&h->tm_h, h->H16, slots, f);
-    if (!tr && s->n_shared) tr = ds4::make_tmap_f16(&h->tm_hs, h->Hs16, M, fs);
+    int tr = ds4::make_act_maps(&h->tm_xp, h->Xp16, slots, d);
+    if (!tr) tr = ds4::make_act_maps(&h->tm_xs, h->Xs16, M, d);
+    if (!tr) tr = ds4::make_act_maps(&h->tm_h, h->H16, slots, f);
+    if (!tr && s->n_shared) tr = ds4::make_act_maps(&h->tm_hs, h->Hs16, M, fs);
     if (tr) DS4_TRY(fail(DS4MOE_ERR_CUDA, "tensor map encoding failed (%d)", tr));
     DS4_TRY(check_q2k_scales(h));
     DS4_TRY(h->alloc_t(&h->router_w3, (size_t)3 * E * d * 2));

@@ -17,7 +17,7 @@
 //   warp 1     allocates TMEM; the converged warp runs the MMA loop and one elected lane issues
 //              the tcgen05.mma and commits of every stage;
 //   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
-//              K stage;
+//              K stage, in 128-row boxes and at most one 64-row box;
 //   warps 3-18 dequantize, in one group per K stage of a raw unit (four groups of four warps for
 //              Q2_K, two of eight for Q8_0) taking the stages round-robin: each warp turns its
 //              16-row groups' 64-wide K stage into fp16 weights in registers (exact small-integer
@@ -259,7 +259,8 @@ __device__ __forceinline__ void deq_q80_stage(uint32_t unit, int su, uint32_t a_
 }
 
 template <int FMT, bool GATEUP>
-__global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
+__global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap64,
+                                                                      const __grid_constant__ CUtensorMap tmap128,
                                                                       GemmArgs p) {
   using C = Cfg<FMT>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -345,9 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
           const int sb = gs % STAGES;
           if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
-          mbar_expect_tx(&b.full[sb], t.nbox * BOX_ROWS * BK * 2);
-          for (int bx = 0; bx < t.nbox; ++bx)
-            tma_load_2d(bdst + bx * BOX_ROWS * BK * 2, &tmap_b, sB * BK, t.row0 + bx * BOX_ROWS, &b.full[sb]);
+          const int rows = t.nbox * BOX_ROWS;  // rows fetched: 128-row boxes, then a 64-row one
+          mbar_expect_tx(&b.full[sb], rows * BK * 2);
+          int r = 0;
+          for (; rows - r >= 2 * BOX_ROWS; r += 2 * BOX_ROWS)
+            tma_load_2d(bdst + r * BK * 2, &tmap128, sB * BK, t.row0 + r, &b.full[sb]);
+          if (r < rows) tma_load_2d(bdst + r * BK * 2, &tmap64, sB * BK, t.row0 + r, &b.full[sb]);
         }
       }
       for (uint32_t k = gs > (uint32_t)STAGES ? gs - STAGES : 0; k < gs; ++k)
@@ -502,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 }
 
 template <int FMT, bool GATEUP>
-cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
-  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm, p);
+cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
+  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm.r64, tm.r128, p);
   return cudaGetLastError();
 }
 
@@ -527,7 +531,7 @@ cudaError_t gemm_prepare() {
 
 // Persistent launch: one CTA per SM (at most), each looping over the (token tile, weight slice)
 // items; n_tiles bounds the token tiles (the routed count itself is read on the device).
-cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmArgs& args, int m_tiles, int n_tiles,
+cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& args, int m_tiles, int n_tiles,
                         cudaStream_t s) {
   static int n_sm[64] = {};
   int dev = 0;
@@ -541,9 +545,9 @@ cudaError_t launch_gemm(int fmt, bool gateup, const CUtensorMap& tm, const GemmA
   return gateup ? launch_one<FMT_Q8_0, true>(tm, p, grid, s) : launch_one<FMT_Q8_0, false>(tm, p, grid, s);
 }
 
-// fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x 64 rows with
-// the 128-byte swizzle (the K-major canonical layout of the MMA's B operand).
-int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols) {
+// fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x box_rows rows
+// with the 128-byte swizzle (the K-major canonical layout of the MMA's B operand).
+int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q;
@@ -555,12 +559,17 @@ int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t col
   }
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {BK, BOX_ROWS};
+  const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+int make_act_maps(ActMaps* tm, const void* base, uint64_t rows, uint64_t cols) {
+  const int r = make_tmap_f16(&tm->r64, base, rows, cols, BOX_ROWS);
+  return r ? r : make_tmap_f16(&tm->r128, base, rows, cols, 2 * BOX_ROWS);
 }
 
 }  // namespace ds4
