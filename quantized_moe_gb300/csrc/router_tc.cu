@@ -6,24 +6,29 @@
 // step go into a fresh fp32 accumulator, which is added to the running sum with ordinary fp32
 // adds: the accuracy of fp32 FMAs on the CUDA cores, at tensor-core throughput.
 //
-// CTA = 64 tokens x 64 experts, 16 warps (each 16 tokens x 16 experts: enough warps per SM to
-// hide the MMA -> add chains); K staged through shared memory 32 at a time in a four-deep
-// cp.async pipeline (three steps of loads in flight).
+// CTA = TT tokens x 64 experts, one warp per 16 tokens x 16 experts (TT = 96 gives 24 warps:
+// enough per SM to hide the MMA -> add chains); K staged through shared memory 32 at a time in a
+// four-deep cp.async pipeline (three steps of loads in flight). TT is chosen per call from the
+// token count so that the grid fills the SMs in as few rounds as possible; every logit is the
+// same sequence of operations whatever the tile, so the result does not depend on TT.
 #include "common.cuh"
 
 namespace ds4 {
 namespace {
 
-constexpr int TT = 64, TE = 64, KS = 32;
-constexpr int kThreads = 512;  // 16 warps: 4 token groups x 4 expert groups
+constexpr int TE = 64, KS = 32;
 constexpr int PAD = 8;  // bf16 elements of padding per shared row (keeps ldmatrix conflict-free)
 constexpr int LDS = KS + PAD;
 constexpr int NSTAGE = 4;
+template <int TT>
 struct Stage {
   __nv_bfloat16 x[TT][LDS];
   __nv_bfloat16 w[3][TE][LDS];
 };
-constexpr int kSmem = NSTAGE * (int)sizeof(Stage);
+template <int TT>
+constexpr int smem_bytes() { return NSTAGE * (int)sizeof(Stage<TT>); }
+template <int TT>
+constexpr int threads_of() { return TT / 16 * (TE / 16) * 32; }  // warps: token groups x expert groups
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool pred) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -51,30 +56,33 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 // w3: [3][E][d] bf16 parts of the router weights
-__global__ void __launch_bounds__(kThreads) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
-                                                        const __nv_bfloat16* __restrict__ w3, const float* __restrict__ b,
-                                                        int n_exp, float* __restrict__ logits) {
+template <int TT>
+__global__ void __launch_bounds__(threads_of<TT>()) router_tc_kernel(const __nv_bfloat16* __restrict__ x, int n_tok,
+                                                                     int d, const __nv_bfloat16* __restrict__ w3,
+                                                                     const float* __restrict__ b, int n_exp,
+                                                                     float* __restrict__ logits) {
+  constexpr int kThreads = threads_of<TT>(), NTG = TT / 16, CPR = KS / 8;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Stage* st = reinterpret_cast<Stage*>(smem_raw);
+  Stage<TT>* st = reinterpret_cast<Stage<TT>*>(smem_raw);
   const int t0 = blockIdx.x * TT, e0 = blockIdx.y * TE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t plane = (size_t)n_exp * d;
   auto stage = [&](int buf, int k0) {
-    // 64 rows x 32 k = 256 chunks of 16 bytes for x, 3 x 256 for the weight parts
-    for (int c = threadIdx.x; c < 4 * TT * (KS / 8); c += kThreads) {
-      const int which = c / (TT * (KS / 8)), r = (c / (KS / 8)) % TT, kc = c % (KS / 8);
-      if (which == 0) {
-        const int t = t0 + r;
-        cp_async16(&st[buf].x[r][kc * 8], x + (size_t)min(t, n_tok - 1) * d + k0 + kc * 8, t < n_tok);
+    // TT rows of x and 3 x 64 rows of weight parts, 32 k = 4 chunks of 16 bytes each
+    for (int c = threadIdx.x; c < (TT + 3 * TE) * CPR; c += kThreads) {
+      const int row = c / CPR, kc = c % CPR;
+      if (row < TT) {
+        const int t = t0 + row;
+        cp_async16(&st[buf].x[row][kc * 8], x + (size_t)min(t, n_tok - 1) * d + k0 + kc * 8, t < n_tok);
       } else {
-        const int e = e0 + r;
-        cp_async16(&st[buf].w[which - 1][r][kc * 8], w3 + (which - 1) * plane + (size_t)min(e, n_exp - 1) * d + k0 + kc * 8,
+        const int which = (row - TT) / TE, r = (row - TT) % TE, e = e0 + r;
+        cp_async16(&st[buf].w[which][r][kc * 8], w3 + which * plane + (size_t)min(e, n_exp - 1) * d + k0 + kc * 8,
                    e < n_exp);
       }
     }
     cp_async_commit();
   };
-  const int tw = warp & 3, ew = warp >> 2;  // token group (16 tokens), expert group (16 experts)
+  const int tw = warp % NTG, ew = warp / NTG;  // token group (16 tokens), expert group (16 experts)
   float acc[2][4];
 #pragma unroll
   for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -151,15 +159,50 @@ void launch_router_split(const float* w, size_t n, __nv_bfloat16* w3, cudaStream
   split3_kernel<<<152 * 4, 256, 0, s>>>(w, n, w3);
 }
 
-void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
-                      float* logits, cudaStream_t s) {
-  dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
+namespace {
+template <int TT>
+void launch_tt(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
+               float* logits, cudaStream_t s) {
+  const dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
   static bool attr_set = false;  // per process; the attribute belongs to the function
   if (!attr_set) {
-    cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaFuncSetAttribute(router_tc_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TT>());
     attr_set = true;
   }
-  router_tc_kernel<<<grid, kThreads, kSmem, s>>>(x, n_tok, d, w3, b, n_exp, logits);
+  router_tc_kernel<TT><<<grid, threads_of<TT>(), smem_bytes<TT>(), s>>>(x, n_tok, d, w3, b, n_exp, logits);
+}
+}  // namespace
+
+// Token tile: the one with the fewest rounds of CTAs over the SMs, weighting a CTA's time by
+// TT + 32 (its weight tile costs about as much as 32 tokens), larger tiles winning ties.
+int router_tile_tokens(int n_tok, int n_exp, int n_sm) {
+  static const int cand[4] = {96, 64, 32, 16};
+  int best = 64;
+  long best_cost = -1;
+  for (int tt : cand) {
+    const long ctas = (long)((n_tok + tt - 1) / tt) * ((n_exp + TE - 1) / TE);
+    const long cost = (ctas + n_sm - 1) / n_sm * (tt + 32);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = tt;
+    }
+  }
+  return best;
+}
+
+void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
+                      float* logits, cudaStream_t s) {
+  static int n_sm[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !n_sm[dev]) cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = (dev >= 0 && dev < 64 && n_sm[dev] > 0) ? n_sm[dev] : 152;
+  switch (router_tile_tokens(n_tok, n_exp, sms)) {
+    case 96: launch_tt<96>(x, n_tok, d, w3, b, n_exp, logits, s); break;
+    case 32: launch_tt<32>(x, n_tok, d, w3, b, n_exp, logits, s); break;
+    case 16: launch_tt<16>(x, n_tok, d, w3, b, n_exp, logits, s); break;
+    default: launch_tt<64>(x, n_tok, d, w3, b, n_exp, logits, s); break;
+  }
 }
 
 }  // namespace ds4
