@@ -24,6 +24,12 @@ SMALL_Q8_NOSHARED = synthetic.Spec("small-q8-noshared", d=384, n_experts=12, top
                                    n_tokens=21, seed=22)
 MIXED_FMT = synthetic.Spec("mixed-fmt", d=512, n_experts=8, top_k=2, f=256, f_shared=256, n_shared=1,
                            fmt_gate_up="q8_0", fmt_down="q2_k", fmt_shared="q2_k", n_tokens=9, seed=23)
+# Zipf-skewed routing over 16 experts: the busiest experts take 700, 673, 550, 355, 230 ... of the
+# 700 tokens, so each spans several token tiles of the expert GEMM with a ragged last tile, and
+# the shared expert's 700 tokens end in a ragged tile as well.
+SKEWED = synthetic.Spec("skewed-multitile", d=512, n_experts=16, top_k=4, f=512, f_shared=256, n_shared=1,
+                        fmt_gate_up="q2_k", fmt_down="q2_k", fmt_shared="q8_0", n_tokens=700, seed=24,
+                        bias="zipf")
 
 
 def check_route(ref, idx, w, n_hash, k):
@@ -114,3 +120,11 @@ def test_distinct_experts_and_counts_match_oracle():
     assert st["counts"][:spec.n_experts].tolist() == counts.tolist()
     assert st["distinct_experts"] == int((counts > 0).sum())
     assert st["error_flags"] == 0
+
+
+def test_experts_spanning_several_token_tiles_match_oracle():
+    p, got, idx, w, ref = _run(SKEWED)
+    counts = np.bincount(idx.ravel(), minlength=SKEWED.n_experts)
+    assert counts.max() > 512  # more than two tiles even at the widest token tile (256)
+    exempt = check_route(ref, idx, w, SKEWED.n_hash, SKEWED.top_k)
+    check_out(p, got, ref, list(range(SKEWED.n_tokens)), idx, exempt)
