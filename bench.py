@@ -81,18 +81,29 @@ def forward_flops(spec) -> float:
     return spec.n_tokens * (spec.top_k * per_pair + shared) + learned * 2.0 * spec.n_experts * spec.d
 
 
-def kernel_source_hash() -> str:
+# Source files that decide each timed kernel's code: a recorded DRAM traffic figure stays valid
+# while these files are unchanged.
+KERNEL_SOURCES = {
+    "decode": ("decode.cu", "mma_units.cuh", "common.cuh"),
+    "gemm": ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh"),
+}
+TRAFFIC_FAMILY = {"route": "decode", "gateup": "decode", "down_combine": "decode",
+                  "routed_gateup": "gemm", "shared_gateup": "gemm", "routed_down": "gemm", "shared_down": "gemm"}
+
+
+def kernel_source_hash(family: str | None = None) -> str:
+    """sha256 prefix over the CUDA sources: all of csrc, or one kernel family's files."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_moe_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + fh.read())
+    names = KERNEL_SOURCES[family] if family else sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """dram bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    """dram bytes per launch from the committed ncu summary, if taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -100,7 +111,8 @@ def recorded_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     ent = rec.get(f"{workload}:{kernel}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    fam = TRAFFIC_FAMILY.get(kernel)
+    if not ent or not fam or ent.get("source_hash") != kernel_source_hash(fam):
         return None
     return ent.get("dram_bytes_per_launch")
 
