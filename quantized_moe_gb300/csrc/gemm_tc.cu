@@ -1,8 +1,7 @@
 // Prefill expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
 // Persistent: one CTA per SM loops over work items, each a 128-row x N-token tile of one expert
-// (N <= 192 tokens for Q2_K weights, <= 256 for Q8_0; the MMA's N is the token count rounded up
-// to 16):
+// (N <= 192 tokens; the MMA's N is the token count rounded up to 16):
 //   gate/up: the 128 rows interleave 64 gate rows and the 64 up rows of the same features, so
 //            the epilogue forms h = silu(g) * u for 64 features and writes it as fp16;
 //   down:    128 rows of d, written as fp32 per bucketed slot for the fixed-order combine.
@@ -10,7 +9,7 @@
 // accumulator is double-buffered in TMEM (2 x 256 columns), so the epilogue of one item overlaps
 // the main loop of the next. Each K stage (64 wide) has one full barrier, completed by the
 // dequant group that wrote its A tile and by the activation TMA, and one empty barrier, completed
-// by the MMA commit.
+// by the MMA commit; four stages are in flight.
 // Warp roles (23 warps):
 //   warp 0     weight producer: bulk-copies the packed weight units of each K unit (256 k for
 //              Q2_K, 128 k for Q8_0) of the tile's rows;
@@ -50,22 +49,23 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;  // double-buffered: the epilogue of one
 
 // Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
 // Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
-#ifndef GEMM_Q2K_STAGES
-#define GEMM_Q2K_STAGES 4
+// Four K stages of 64 (A and B tiles) with token tiles of 192.
+#ifndef GEMM_STAGES
+#define GEMM_STAGES 4
 #endif
-#ifndef GEMM_Q2K_BN
-#define GEMM_Q2K_BN 192
+#ifndef GEMM_BN
+#define GEMM_BN 192
 #endif
 template <int FMT>
 struct Cfg {
   static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);
   static constexpr int RAWS = FMT == FMT_Q2_K ? 4 : 3;
-  // Token tile (MMA N at most): Q2_K takes 192 tokens so that four K stages fit in shared memory,
-  // Q8_0 (larger raw units) 256 with three.
-  static constexpr int BN = FMT == FMT_Q2_K ? GEMM_Q2K_BN : 256;
+  // Token tile (MMA N at most): 192 tokens, so that four K stages fit in shared memory beside the
+  // raw weight stages.
+  static constexpr int BN = GEMM_BN;
   static constexpr int B_BYTES = BN * BK * 2;
   // K stages in flight: each holds a dequantized weight tile (A) and an activation tile (B)
-  static constexpr int STAGES = FMT == FMT_Q2_K ? GEMM_Q2K_STAGES : 3;
+  static constexpr int STAGES = GEMM_STAGES;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
