@@ -1,0 +1,202 @@
+"""A model of the expert GEMM's barrier protocol, checked on the CPU.
+
+The persistent tcgen05 GEMM (csrc/gemm_tc.cu) runs four kinds of actors over mbarriers whose
+waits test only the parity of a phase: the weight producer (raw units, rings of RAWS), the
+activation producer, NG dequant groups that take the K stages round-robin, and the MMA issuer,
+whose commits complete in issue order. A wait for phase k is sound only while the barrier is at
+phase k or k + 1: if it is still at phase k - 1, that phase has the other parity and the wait
+returns at once, before phase k has even begun. An arrival meant for phase k that lands while an
+earlier phase is still open is counted in that earlier phase. A variant with more A stages than
+B stages, whose dequant groups wait for the activation tile, runs into exactly this (the last
+test shows it), and on the GPU it faulted.
+
+This model replays the committed protocol under random interleavings and random completion
+delays and asserts, for every wait, that its barrier had reached the phase it waits for (no
+parity aliasing) and, for every arrival, that it lands in the phase it belongs to. The
+constants are the kernel's: four K stages in flight, raw rings of four (Q2_K) and three (Q8_0)
+units, one dequant group per K stage of a raw unit (four for Q2_K's 256-wide units, two for
+Q8_0's 128-wide ones).
+"""
+import random
+
+import pytest
+
+
+class Violation(AssertionError):
+    pass
+
+
+class Bar:
+    """An mbarrier: `expected` arrivals per phase, plus transaction bytes that must land too."""
+
+    def __init__(self, name, expected):
+        self.name, self.expected = name, expected
+        self.phase = 0          # index of the phase in progress (= completed phases)
+        self.arrived = 0
+        self.tx_pending = 0
+
+    def arrive(self, k, tx=0):
+        if self.phase != k:
+            raise Violation(f"{self.name}: arrival for phase {k} while phase {self.phase} is open")
+        self.arrived += 1
+        self.tx_pending += tx
+        self._maybe_complete()
+
+    def land(self, k):
+        if self.phase != k:
+            raise Violation(f"{self.name}: bytes for phase {k} landed in phase {self.phase}")
+        self.tx_pending -= 1
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.arrived == self.expected and self.tx_pending == 0:
+            self.phase += 1
+            self.arrived = 0
+
+    def done(self, k):
+        """A wait for phase k (k < 0: the slot's first use, nothing to wait for)."""
+        return k < 0 or self.phase > k
+
+    def check_wait(self, k):
+        # the kernel polls the parity of phase k: that is sound only while the barrier is at phase
+        # k (in progress) or k + 1 (just completed); two phases off, the parity answers wrongly
+        if k >= 0 and not (k <= self.phase <= k + 1):
+            raise Violation(f"{self.name}: wait for phase {k} began at phase {self.phase} (parity alias)")
+
+
+def simulate(ng, stages, raws, n_items, stages_per_item, seed, skip_empty_wait=False, b_stages=None):
+    """b_stages=None: the committed protocol (one full/empty pair per stage for A and B).
+    b_stages=n: the variant with separate A (`stages`) and B (`n`) rings, in which the first
+    dequant warp of a group waits for the stage's B tile before handing the stage to the MMA."""
+    rng = random.Random(seed)
+    kpu = ng  # stages per raw unit: each group takes exactly one stage of every unit
+    n_stages = n_items * stages_per_item
+    n_units = n_stages // kpu
+    split = b_stages is not None
+    full = [Bar(f"full[{i}]", 1 if split else 2) for i in range(stages)]  # group (+ producer, + bytes)
+    empty = [Bar(f"empty[{i}]", 1) for i in range(stages)]     # MMA commit
+    bfull = [Bar(f"b_full[{i}]", 1) for i in range(b_stages)] if split else full
+    bempty = [Bar(f"b_empty[{i}]", 1) for i in range(b_stages)] if split else empty
+    nb = b_stages if split else stages
+    raw_full = [Bar(f"raw_full[{i}]", 1) for i in range(raws)]  # weight producer (+ bytes)
+    raw_empty = [Bar(f"raw_empty[{i}]", ng) for i in range(raws)]  # one arrival per group
+    pending = []  # (kind, target, phase) asynchronous completions: copies landing, MMAs finishing
+
+    def weight_producer():
+        for u in range(n_units):
+            b = raw_empty[u % raws]
+            k = u // raws - 1
+            b.check_wait(k)
+            while not b.done(k):
+                yield
+            raw_full[u % raws].arrive(u // raws, tx=1)
+            pending.append(("land", raw_full[u % raws], u // raws))
+            yield
+
+    def act_producer():
+        for g in range(n_stages):
+            b = bempty[g % nb]
+            k = g // nb - 1
+            b.check_wait(k)
+            while not b.done(k):
+                yield
+            bfull[g % nb].arrive(g // nb, tx=1)
+            pending.append(("land", bfull[g % nb], g // nb))
+            yield
+
+    def dequant(grp):
+        for g in range(grp, n_stages, ng):
+            u = g // kpu
+            rb = raw_full[u % raws]
+            rb.check_wait(u // raws)
+            while not rb.done(u // raws):
+                yield
+            if not skip_empty_wait:
+                eb = empty[g % stages]
+                k = g // stages - 1
+                eb.check_wait(k)
+                while not eb.done(k):
+                    yield
+            for _ in range(rng.randint(0, 3)):  # dequantization takes a while
+                yield
+            if split:  # the fold: B of this stage must have landed before the hand-over
+                bb = bfull[g % nb]
+                bb.check_wait(g // nb)
+                while not bb.done(g // nb):
+                    yield
+            full[g % stages].arrive(g // stages)
+            raw_empty[u % raws].arrive(u // raws)
+            yield
+
+    mma_inflight = []
+
+    def mma():
+        for g in range(n_stages):
+            fb = full[g % stages]
+            fb.check_wait(g // stages)
+            while not fb.done(g // stages):
+                yield
+            mma_inflight.append(g)  # the commit arrives when this and every earlier MMA completes
+            yield
+
+    actors = [weight_producer(), act_producer(), mma()] + [dequant(j) for j in range(ng)]
+    steps = 0
+    while actors or pending or mma_inflight:
+        steps += 1
+        if steps > 200000:
+            raise Violation("no progress (deadlock)")
+        r = rng.random()
+        if pending and r < 0.25:
+            kind, bar, k = pending.pop(rng.randrange(len(pending)))
+            bar.land(k)
+            continue
+        if mma_inflight and r < 0.45:
+            g = mma_inflight.pop(0)  # in order
+            empty[g % stages].arrive(g // stages)
+            if split:
+                bempty[g % nb].arrive(g // nb)
+            continue
+        if actors:
+            a = rng.choice(actors)
+            try:
+                next(a)
+            except StopIteration:
+                actors.remove(a)
+    return full, empty, raw_full, raw_empty
+
+
+@pytest.mark.parametrize("fmt,ng,stages,raws", [("q2_k", 4, 4, 4), ("q8_0", 2, 4, 3)])
+def test_committed_protocol_has_no_parity_alias(fmt, ng, stages, raws):
+    for seed in range(150):
+        full, empty, raw_full, raw_empty = simulate(ng, stages, raws, n_items=3, stages_per_item=4 * ng, seed=seed)
+        n_stages = 3 * 4 * ng
+        # every stage went through its barriers exactly once
+        assert sum(b.phase for b in full) == n_stages
+        assert sum(b.phase for b in empty) == n_stages
+        assert sum(b.phase for b in raw_full) == n_stages // ng
+
+
+def test_model_catches_a_group_that_skips_the_empty_wait():
+    # without the wait on the stage's release a dequant group arms a barrier phase that is
+    # still open: the model must see it
+    caught = 0
+    for seed in range(50):
+        try:
+            simulate(4, 4, 4, n_items=3, stages_per_item=16, seed=seed, skip_empty_wait=True)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+def test_split_rings_are_sound_only_with_no_more_a_than_b_stages():
+    # equal rings: sound
+    for seed in range(100):
+        simulate(4, 4, 4, n_items=3, stages_per_item=16, seed=seed, b_stages=4)
+    # six A stages over three B stages: the B wait of a group can start two phases behind
+    caught = 0
+    for seed in range(100):
+        try:
+            simulate(4, 6, 4, n_items=3, stages_per_item=16, seed=seed, b_stages=3)
+        except Violation:
+            caught += 1
+    assert caught > 0
