@@ -187,3 +187,23 @@ def test_q2k_scale_beyond_fp16_dequant_range_is_refused():
     assert ei.value.code == api.DS4MOE_ERR_UNSUPPORTED_FORMAT
     h = moe_gpu.create(q, max_tokens=4)  # decode path only: no fp16 dequant, accepted
     api.ds4moe_destroy(h)
+
+
+def test_batched_forward_with_every_token_table_routed():
+    """Whole-layer table routing (every token hash-routed, as in a model's first layers): the
+    batched path runs without the router, and matches the oracle."""
+    p = synthetic.make_problem(SMALL_MIX)
+    n = 40  # above the decode limit: the batched path
+    tids = np.random.default_rng(31).integers(0, SMALL_MIX.hash_vocab, n).astype(np.int32)
+    xb = synthetic.activations(SMALL_MIX, n)
+    h = moe_gpu.create(p, max_tokens=n)
+    try:
+        got, idx, w = moe_gpu.forward(h, p, x_bits=xb, n_hash=n, token_ids=tids)
+        st = api.ds4moe_get_stats(h)
+    finally:
+        api.ds4moe_destroy(h)
+    ref = moe.forward(p, x_bits=xb, token_ids=tids, n_hash=n)
+    assert np.array_equal(idx, ref["idx"])
+    assert np.all(w == np.float32(1.0 / SMALL_MIX.top_k))
+    assert int(st["counts"].sum()) == n * SMALL_MIX.top_k and st["error_flags"] == 0
+    assert np.max(np.abs(got - ref["out"])) <= moe_gpu.tolerance(ref["out"])
