@@ -10,8 +10,9 @@ earlier phase is still open is counted in that earlier phase. A variant with mor
 B stages, whose dequant groups wait for the activation tile, runs into exactly this (the last
 test shows it), and on the GPU it faulted.
 
-This model replays the committed protocol under random interleavings and random completion
-delays and asserts, for every wait, that its barrier had reached the phase it waits for (no
+This model replays the committed protocol (stage rings, raw weight rings and the two TMEM
+accumulator buffers between the MMA issuer and the epilogue) under random interleavings and
+random completion delays and asserts, for every wait, that its barrier had reached the phase it waits for (no
 parity aliasing) and, for every arrival, that it lands in the phase it belongs to. The
 constants are the kernel's: four K stages in flight, raw rings of four (Q2_K) and three (Q8_0)
 units, one dequant group per K stage of a raw unit (four for Q2_K's 256-wide units, two for
@@ -80,6 +81,8 @@ def simulate(ng, stages, raws, n_items, stages_per_item, seed, skip_empty_wait=F
     nb = b_stages if split else stages
     raw_full = [Bar(f"raw_full[{i}]", 1) for i in range(raws)]  # weight producer (+ bytes)
     raw_empty = [Bar(f"raw_empty[{i}]", ng) for i in range(raws)]  # one arrival per group
+    acc_full = [Bar(f"acc_full[{i}]", 1) for i in range(2)]     # MMA commit after an item's last stage
+    acc_empty = [Bar(f"acc_empty[{i}]", 1) for i in range(2)]   # the epilogue has read the accumulator
     pending = []  # (kind, target, phase) asynchronous completions: copies landing, MMAs finishing
 
     def weight_producer():
@@ -131,15 +134,37 @@ def simulate(ng, stages, raws, n_items, stages_per_item, seed, skip_empty_wait=F
     mma_inflight = []
 
     def mma():
-        for g in range(n_stages):
-            fb = full[g % stages]
-            fb.check_wait(g // stages)
-            while not fb.done(g // stages):
+        g = 0
+        for item in range(n_items):
+            buf, k = item & 1, (item >> 1) - 1  # the epilogue has drained item - 2's buffer
+            ab = acc_empty[buf]
+            ab.check_wait(k)
+            while not ab.done(k):
                 yield
-            mma_inflight.append(g)  # the commit arrives when this and every earlier MMA completes
+            for _ in range(stages_per_item):
+                fb = full[g % stages]
+                fb.check_wait(g // stages)
+                while not fb.done(g // stages):
+                    yield
+                mma_inflight.append(("stage", g))  # commits arrive when every earlier MMA completes
+                g += 1
+                yield
+            mma_inflight.append(("acc", item))
             yield
 
-    actors = [weight_producer(), act_producer(), mma()] + [dequant(j) for j in range(ng)]
+    def epilogue():
+        for item in range(n_items):
+            buf, k = item & 1, item >> 1
+            ab = acc_full[buf]
+            ab.check_wait(k)
+            while not ab.done(k):
+                yield
+            for _ in range(rng.randint(0, 6)):  # reading TMEM, SwiGLU, stores
+                yield
+            acc_empty[buf].arrive(k)
+            yield
+
+    actors = [weight_producer(), act_producer(), mma(), epilogue()] + [dequant(j) for j in range(ng)]
     steps = 0
     while actors or pending or mma_inflight:
         steps += 1
@@ -151,10 +176,13 @@ def simulate(ng, stages, raws, n_items, stages_per_item, seed, skip_empty_wait=F
             bar.land(k)
             continue
         if mma_inflight and r < 0.45:
-            g = mma_inflight.pop(0)  # in order
-            empty[g % stages].arrive(g // stages)
+            kind, v = mma_inflight.pop(0)  # in order
+            if kind == "acc":
+                acc_full[v & 1].arrive(v >> 1)
+                continue
+            empty[v % stages].arrive(v // stages)
             if split:
-                bempty[g % nb].arrive(g // nb)
+                bempty[v % nb].arrive(v // nb)
             continue
         if actors:
             a = rng.choice(actors)
@@ -162,6 +190,7 @@ def simulate(ng, stages, raws, n_items, stages_per_item, seed, skip_empty_wait=F
                 next(a)
             except StopIteration:
                 actors.remove(a)
+    assert [b.phase for b in acc_empty] == [(n_items + 1 - i) // 2 for i in range(2)]
     return full, empty, raw_full, raw_empty
 
 
