@@ -7,9 +7,12 @@ steps (a write of twice the L2 size, outside the timed events). Prints one JSON 
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
---config picks the workload (default 1: decode of one token, d=4096, 256 experts, top-8,
-f=2048, Q2_K routed + Q8_0 shared). Under torchrun each rank runs an independent replica on
-its own tokens (weak scaling, no collective on the data path).
+--config picks the headline workload (default 4: prefill of 4096 tokens, d=4096, 256 experts,
+top-8, f=2048, Q2_K routed + Q8_0 shared, the first 1024 tokens table-routed: the largest
+single-GPU workload, tensor-core bound). Every other workload (tiny-q8, decode-1, decode-16,
+prefill-512) is timed in the same run and reported under detail.per_config, each with its own
+roofline (HBM for decode). Under torchrun each rank runs an independent replica on its own
+tokens (weak scaling, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -249,45 +252,33 @@ def whole_job_rate(world: int, tokens_per_step: int, steps: int, seconds: float)
 
 # ------------------------------------------------------------------ GPU arm
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batches", type=int, default=8, help="distinct input batches cycled over the steps")
-    ap.add_argument("--l2-mode", choices=["layer", "flush"], default="layer",
-                    help="between steps: flush L2 then run a second layer (default), or flush only")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+def kernel_work(spec, distinct: float) -> dict:
+    """Algorithmic work of each timed phase: bytes (decode path, HBM-bound) or FLOPs (expert GEMMs)."""
+    wb = weight_bytes(spec, distinct)
+    pair = 2.0 * spec.d * spec.f
+    nb = {"routed_gateup": wb["routed_gateup"] + wb["x"], "routed_down": wb["routed_down"],
+          "shared_gateup": wb["shared"] * 2 / 3 + wb["x"], "shared_down": wb["shared"] / 3,
+          "router_logits": wb["router"] + wb["x"], "combine": wb["out"],
+          # decode path: route; gate/up of the touched and the shared experts; down + combine
+          "route": wb["router"] + wb["x"],
+          "gateup": wb["routed_gateup"] + wb["shared"] * 2 / 3 + wb["x"],
+          "down_combine": wb["routed_down"] + wb["shared"] / 3 + wb["out"]}
+    fl = {"routed_gateup": spec.n_tokens * spec.top_k * 2 * pair, "routed_down": spec.n_tokens * spec.top_k * pair,
+          "shared_gateup": spec.n_tokens * 2 * 2.0 * spec.d * spec.f_shared,
+          "shared_down": spec.n_tokens * 2.0 * spec.d * spec.f_shared}
+    return dict(bytes=nb, flops=fl, weights=wb)
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    spec = synthetic.CONFIGS[args.config]
 
-    if args.impl == "reference":
-        run_reference(args, spec, rank)
-        return
-
+def measure(api, spec, args, dev, stream, rank, world, peaks, l2_mode, with_e2e=True):
+    """Creates the workload's handle (and, in `layer` mode, a second layer), times K forwards with
+    CUDA events (L2 prepared between steps, outside the events), then a profiled pass (per-launch
+    times) and the end-to-end host-buffer pass. Returns a dict of raw measurements."""
     import torch
-    import torch.distributed as dist
-    from quantized_moe_gb300 import ds4moe as api
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    peaks = load_peaks()
 
     problem = synthetic.make_problem(spec)
     shapes = api.make_shapes(spec.d, spec.f, spec.f_shared, spec.n_experts, spec.top_k, spec.n_shared,
                              spec.fmt_gate_up, spec.fmt_down, spec.fmt_shared, problem.router_b is not None,
-                             spec.hash_vocab, spec.n_tokens, local)
+                             spec.hash_vocab, spec.n_tokens, dev.index)
     arrays = [problem.router_w, problem.router_b, problem.gate.full(), problem.up.full(), problem.down.full(),
               problem.shared_gate, problem.shared_up, problem.shared_down, problem.hash_table]
     h = api.ds4moe_create(api.make_weights(*arrays), shapes)
@@ -296,7 +287,7 @@ def main():
     # after the L2 flush, as the previous layer of a model would, so the kernels' code is warm
     # while every byte of the timed layer's data is cold.
     h_prev = None
-    if args.l2_mode == "layer":
+    if l2_mode == "layer":
         pp = synthetic.make_problem(spec.with_(seed=spec.seed + 1000003))
         arrays = [pp.router_w, pp.router_b, pp.gate.full(), pp.up.full(), pp.down.full(), pp.shared_gate,
                   pp.shared_up, pp.shared_down, pp.hash_table]
@@ -312,10 +303,9 @@ def main():
             r = np.random.default_rng(sb.seed)
             tids.append(torch.from_numpy(r.integers(0, spec.hash_vocab, spec.n_hash).astype(np.int32)).to(dev))
     out = torch.empty((spec.n_tokens, spec.d), dtype=torch.float32, device=dev)
+    out_prev = torch.empty_like(out)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
-
-    out_prev = torch.empty_like(out)
 
     def fwd(i, handle=None, o=None):
         b = i % args.batches
@@ -344,12 +334,12 @@ def main():
         fwd(i)
     torch.cuda.synchronize()
 
-    # timed region: each step timed alone with events on the launching stream (L2 prepared
-    # before each step as above, outside the events)
-    sampler = ClockSampler(local) if rank == 0 else None
+    # timed region: each step timed alone with events on the launching stream
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
     if sampler:
         sampler.start()
     step_ms = time_steps(args.steps, cool)
@@ -357,8 +347,6 @@ def main():
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
-    value = whole_job_rate(world, spec.n_tokens, args.steps, total_ms / 1e3)
-    ms_per_step = total_ms / args.steps
 
     # per-launch times of the same workload: events recorded between the launches (this
     # serialises the launches, so it runs after the timed region, over the same inputs)
@@ -375,93 +363,155 @@ def main():
     api.ds4moe_set_profiling(h, False)
 
     # end to end through the host entry point: pinned host input, copies inside the timed region
-    x_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.int16, pin_memory=True)
-    x_host.copy_(xs[0].cpu())
-    out_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.float32, pin_memory=True)
-    tid_host = tids[0].cpu().pin_memory() if spec.n_hash else None
-    e2e_s = []
-    for i in range(args.warmup + args.steps):
-        cool(i)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        api.ds4moe_forward_host(h, x_host.data_ptr(), spec.n_tokens, tid_host.data_ptr() if tid_host is not None else None,
-                                spec.n_hash, out_host.data_ptr(), stream.cuda_stream)
-        if i >= args.warmup:
-            e2e_s.append(time.perf_counter() - t0)
-    e2e_total = max_over_ranks(float(sum(e2e_s)), world, dev)
-    e2e_value = whole_job_rate(world, spec.n_tokens, args.steps, e2e_total)
+    e2e_total = None
+    if with_e2e:
+        x_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.int16, pin_memory=True)
+        x_host.copy_(xs[0].cpu())
+        out_host = torch.empty((spec.n_tokens, spec.d), dtype=torch.float32, pin_memory=True)
+        tid_host = tids[0].cpu().pin_memory() if spec.n_hash else None
+        e2e_s = []
+        for i in range(args.warmup + args.steps):
+            cool(i)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            api.ds4moe_forward_host(h, x_host.data_ptr(), spec.n_tokens,
+                                    tid_host.data_ptr() if tid_host is not None else None,
+                                    spec.n_hash, out_host.data_ptr(), stream.cuda_stream)
+            if i >= args.warmup:
+                e2e_s.append(time.perf_counter() - t0)
+        e2e_total = max_over_ranks(float(sum(e2e_s)), world, dev)
 
     launches = api.ds4moe_launches_per_forward(h, spec.n_tokens) * args.steps
     api.ds4moe_destroy(h)
     if h_prev is not None:
         api.ds4moe_destroy(h_prev)
+    del xs, tids, out, out_prev, flush_buf
+    torch.cuda.empty_cache()
+    return dict(problem=problem, step_ms=step_ms, total_ms=total_ms, flush_only_ms=flush_only_ms,
+                phase_ms={k: float(np.mean(v)) for k, v in phase_ms.items()}, distinct=float(np.mean(distinct)),
+                e2e_total=e2e_total, launches=launches, clocks=clocks, l2_layer=h_prev is not None)
+
+
+def summarize(spec, m, args, world, peaks) -> dict:
+    """Throughput and roofline fractions of one measured workload."""
+    ms_per_step = m["total_ms"] / args.steps
+    work = kernel_work(spec, m["distinct"])
+    mean_phase = m["phase_ms"]
+    top = max(mean_phase, key=mean_phase.get)
+    fwd_bytes = sum(work["weights"].values())
+    flops = forward_flops(spec)
+    hbm_bound = spec.n_tokens <= 64 or top not in work["flops"]
+    if hbm_bound:
+        alg = work["bytes"].get(top, 0.0)
+        achieved = alg / (mean_phase[top] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm"], "peak_source": f"{peaks['src']} hbm_gbs",
+                "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(top, spec.name)}
+    else:
+        alg = work["flops"][top]
+        achieved = alg / (mean_phase[top] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"],
+                "peak_source": f"{peaks['src']} bf16_tflops (burst; the fp16 dense rate equals bf16's)",
+                "algorithmic_flops_per_launch": alg, "traffic": recorded_traffic(top, spec.name)}
+    tot = sum(mean_phase.values())
+    return dict(
+        ms_per_step=ms_per_step,
+        value=whole_job_rate(world, spec.n_tokens, args.steps, m["total_ms"] / 1e3),
+        e2e=None if m["e2e_total"] is None else whole_job_rate(world, spec.n_tokens, args.steps, m["e2e_total"]),
+        roofline=roof,
+        detail={"step_ms_p10_p50_p90": [float(np.percentile(m["step_ms"], q)) for q in (10, 50, 90)],
+                "ms_per_step_flush_only": float(np.mean(m["flush_only_ms"])),
+                "phase_ms": mean_phase, "phase_share": {k: v / tot for k, v in mean_phase.items()},
+                "distinct_experts_mean": m["distinct"],
+                "forward_algorithmic_bytes": fwd_bytes, "forward_gbs": fwd_bytes / (ms_per_step / 1e3) / 1e9,
+                "forward_hbm_frac": fwd_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm"],
+                "forward_flops": flops, "forward_tflops": flops / (ms_per_step / 1e3) / 1e12,
+                "forward_tensor_frac": flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16"]})
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4,
+                    help="headline workload (default 4: prefill-4096, the largest single-GPU workload)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the headline workload")
+    ap.add_argument("--batches", type=int, default=8, help="distinct input batches cycled over the steps")
+    ap.add_argument("--l2-mode", choices=["layer", "flush"], default="layer",
+                    help="between steps: flush L2 then run a second layer (default), or flush only")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = synthetic.CONFIGS[args.config]
+
+    if args.impl == "reference":
+        run_reference(args, spec, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from quantized_moe_gb300 import ds4moe as api
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    m = measure(api, spec, args, dev, stream, rank, world, peaks, args.l2_mode)
+    head = summarize(spec, m, args, world, peaks)
+    per_config = {}
+    if not args.no_per_config:
+        for c in sorted(synthetic.CONFIGS):
+            if c == args.config:
+                continue
+            cs = synthetic.CONFIGS[c]
+            mc = measure(api, cs, args, dev, stream, rank, world, peaks, args.l2_mode)
+            sc = summarize(cs, mc, args, world, peaks)
+            per_config[cs.name] = {"workload": workload_name(cs), "value": sc["value"], "unit": "tok/s",
+                                   "ms_per_step": sc["ms_per_step"], "e2e_tok_s": sc["e2e"],
+                                   "roofline": sc["roofline"], "gpu_launches": mc["launches"],
+                                   "clocks": mc["clocks"], **sc["detail"]}
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    # roofline of the dominant kernel (largest share of the stream time)
-    mean_phase = {k: float(np.mean(v)) for k, v in phase_ms.items()}
-    top = max(mean_phase, key=mean_phase.get)
-    d_mean = float(np.mean(distinct))
-    wb = weight_bytes(spec, d_mean)
-    flops = forward_flops(spec)
-    bytes_alg = {"routed_gateup": wb["routed_gateup"] + wb["x"], "routed_down": wb["routed_down"],
-                 "shared_gateup": wb["shared"] * 2 / 3 + wb["x"], "shared_down": wb["shared"] / 3,
-                 "router_logits": wb["router"] + wb["x"], "combine": wb["out"],
-                 # decode path: gate/up of the touched and the shared experts; down + combine
-                 "route": wb["router"] + wb["x"],
-                 "gateup": wb["routed_gateup"] + wb["shared"] * 2 / 3 + wb["x"],
-                 "down_combine": wb["routed_down"] + wb["shared"] / 3 + wb["out"]}
-    decode = spec.n_tokens <= 64
-    if decode:
-        achieved = bytes_alg.get(top, 0.0) / (mean_phase[top] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm"], "peak_source": f"{peaks['src']} hbm_gbs",
-                "algorithmic_bytes_per_launch": bytes_alg.get(top, 0.0),
-                "traffic": recorded_traffic(top, spec.name)}
-    else:
-        pair = 2.0 * spec.d * spec.f
-        fl = {"routed_gateup": spec.n_tokens * spec.top_k * 2 * pair, "routed_down": spec.n_tokens * spec.top_k * pair,
-              "shared_gateup": spec.n_tokens * 2 * 2.0 * spec.d * spec.f_shared,
-              "shared_down": spec.n_tokens * 2.0 * spec.d * spec.f_shared}
-        achieved = fl.get(top, 0.0) / (mean_phase[top] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16"], "peak_source": f"{peaks['src']} bf16_tflops (fp16 dense = bf16 rate)",
-                "algorithmic_flops_per_launch": fl.get(top, 0.0), "traffic": recorded_traffic(top, spec.name)}
-    fwd_bytes = sum(wb.values())
-    share = {k: v / sum(mean_phase.values()) for k, v in mean_phase.items()}
-
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_done, dt = oracle_sample(spec, problem, args.cpu_seconds)
+        n_done, dt = oracle_sample(spec, m["problem"], args.cpu_seconds)
         cpu = {"value": n_done / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
                "sample": f"first {n_done} token(s) of the workload, one at a time, fp64 numpy oracle, 1 thread "
                          f"of {os.cpu_count()} host cores, {dt:.1f} s"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 mma, f32 accumulate", "data": "synthetic",
         "config": {"workload": workload_name(spec),
                    "l2": ("flushed between steps (write of 2x L2), then one forward of a second layer with its own "
                           "weights (kernel code warm, every byte of the timed layer cold)"
-                          if h_prev is not None else "flushed between steps (write of 2x L2)"),
+                          if m["l2_layer"] else "flushed between steps (write of 2x L2)"),
                    "parallelism": f"replicas x{world}", "batches": args.batches},
-        "roofline": roof,
+        "roofline": head["roofline"],
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": spec.n_tokens * spec.d * 2 + spec.n_hash * 4,
+        "e2e": {"value": head["e2e"], "unit": "tok/s",
+                "h2d_bytes_per_step": spec.n_tokens * spec.d * 2 + spec.n_hash * 4,
                 "d2h_bytes_per_step": spec.n_tokens * spec.d * 4},
-        "gpu_launches": launches,
-        "clocks": clocks,
-        "detail": {"step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
-                   "ms_per_step_flush_only": float(np.mean(flush_only_ms)),
-                   "phase_ms": mean_phase, "phase_share": share, "distinct_experts_mean": d_mean,
-                   "forward_algorithmic_bytes": fwd_bytes, "forward_gbs": fwd_bytes / (ms_per_step / 1e3) / 1e9,
-                   "forward_hbm_frac": fwd_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm"],
-                   "forward_flops": flops, "forward_tflops": flops / (ms_per_step / 1e3) / 1e12,
-                   "kernel_source_hash": kernel_source_hash(), "peaks": peaks},
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
+        "detail": {**head["detail"], "kernel_source_hash": kernel_source_hash(), "peaks": peaks,
+                   "per_config": per_config},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

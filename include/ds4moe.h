@@ -53,7 +53,13 @@ extern "C" {
 
 #define DS4MOE_OK 0
 #define DS4MOE_ERR_INVALID_ARG -1        /* null pointer, bad size or shape */
-#define DS4MOE_ERR_UNSUPPORTED_FORMAT -2 /* format enum not Q8_0 / Q2_K, or shape not tileable */
+#define DS4MOE_ERR_UNSUPPORTED_FORMAT -2 /* format enum not Q8_0 / Q2_K, or shape not tileable; also
+                                            a Q2_K super-block with |d| >= 0.0666 (more precisely,
+                                            15 * 2^16 * |d| >= 65504) on a handle whose max_tokens
+                                            enables the batched path (max_tokens > 16 or
+                                            max_tokens * top_k > 128): that path dequantizes Q2_K
+                                            weights in fp16 as q * 2^-16 times 2^16 * d * s. Decode-
+                                            only handles accept any fp16 d */
 #define DS4MOE_ERR_DEVICE_MISMATCH -3    /* a device pointer lives on another GPU than the handle */
 #define DS4MOE_ERR_CAPACITY -4           /* n_tokens > max_tokens given at create */
 #define DS4MOE_ERR_OOM -5                /* device allocation failed or exceeded workspace_limit */
@@ -98,8 +104,23 @@ typedef struct ds4moe_weights {
 typedef struct ds4moe_stats {
     int32_t n_tokens;          /* tokens of the last forward */
     int32_t distinct_experts;  /* routed experts with at least one token in the last forward */
-    int32_t error_flags;       /* bit 0: a token id was outside [0, hash_vocab) (that token's
-                                  routed part was skipped) */
+    int32_t error_flags;       /* device-side conditions of the last forward (0 = none). The
+                                  forward itself has already returned DS4MOE_OK when they arise:
+                                  read them here after a forward whose result matters.
+                                  bit 0: a token id was outside [0, hash_vocab); that token's
+                                         routed part was skipped (weights 0), the rest is valid.
+                                  bit 2: a pipeline wait of the batched expert GEMM gave up after
+                                         its time limit (about one second); the GEMM stopped and
+                                         the output rows of that launch are incomplete. One of
+                                         bits 17..23 names the wait: 17 weight producer (raw slot
+                                         free), 18 activation producer (stage free), 19 dequant
+                                         (raw weights landed), 20 dequant (stage free), 21
+                                         epilogue (accumulator full), 22 MMA (accumulator free),
+                                         23 MMA (stage full).
+                                  bit 3: in the batched path, an intermediate |h| = |silu(g) u|
+                                         exceeded the fp16 range (65504); it was stored as an
+                                         infinity and the affected output rows are not finite.
+                                  Other bits are reserved. */
     int32_t reserved;
     int32_t counts[256];       /* tokens per routed expert in the last forward */
 } ds4moe_stats;
@@ -160,14 +181,17 @@ int ds4moe_get_phase_times(ds4moe_handle* h, float* ms, const char** names, int3
  * it computes fp32 logits of router_w (device fp32 [n_experts x d]) and router_b (device fp32
  * [n_experts] or NULL) for x (device bf16 [n_tokens x d]), then the sigmoid top-k with ties to
  * the lower index and weights renormalised to sum 1, into idx (device int32
- * [n_tokens x top_k]) and w (device fp32 [n_tokens x top_k]), in top-k order -- the same
- * kernels and results as the routing of ds4moe_forward. Runs on the calling thread's current
- * device, asynchronously on stream. The logits live in a static device array of
- * DS4MOE_NOALLOC_MAX_LOGITS floats that the library image carries (held by every GPU that loads
- * the library until exit): n_tokens * n_experts above that returns DS4MOE_ERR_CAPACITY. The
- * first call on a device looks the array's address up (cudaGetSymbolAddress); make it before
- * any stream capture. All calls on a device share the array, so calls that may overlap on the
- * GPU (unordered streams) race. */
+ * [n_tokens x top_k]) and w (device fp32 [n_tokens x top_k]), in top-k order. It computes the
+ * same routing as ds4moe_forward with its own kernel (fp32 FMA logits): the fp32 summation order
+ * differs from the forward's routers, so logits may differ in the last bits, and the chosen
+ * experts agree with the forward's except where the k-th and (k+1)-th scores are within about
+ * 1e-6 of each other. Runs on the calling thread's current device, asynchronously on stream.
+ * The logits live in a static device array of DS4MOE_NOALLOC_MAX_LOGITS floats that the library
+ * image carries (held by every GPU that loads the library until exit): n_tokens * n_experts
+ * above that returns DS4MOE_ERR_CAPACITY. The first call on a device looks the array's address
+ * up (cudaGetSymbolAddress) and sets the router kernel's attributes in that device's context;
+ * make it before any stream capture. All calls on a device share the array, so calls that may
+ * overlap on the GPU (unordered streams) race. */
 #define DS4MOE_NOALLOC_MAX_LOGITS 262144
 int ds4moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int32_t n_tokens,
                          int32_t d, int32_t n_experts, int32_t top_k, int32_t* idx, float* w, void* stream);

@@ -216,6 +216,8 @@ void launch_tiles(const int* counts, const int* offsets, int n_exp, int tile_n, 
 void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s);
 void launch_q2k_dmax(const uint8_t* packed, size_t bytes, unsigned* out, cudaStream_t s);
 void launch_router_split(const float* w, size_t n, __nv_bfloat16* w3, cudaStream_t s);
+cudaError_t router_tc_prepare();      // kernel attributes, once per device (not inside a capture)
+cudaError_t router_logits_prepare();  // the same for the scalar router
 void launch_router_tc(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
                       float* logits, cudaStream_t s);
 void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float* w, const float* b, int n_exp,

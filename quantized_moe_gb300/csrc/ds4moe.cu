@@ -153,9 +153,6 @@ struct ds4moe_handle {
     const int* tid = nullptr;
     float* out = nullptr;
   };
-  static constexpr int kPinned = 16;
-  const void* pinned[kPinned] = {};  // host addresses known to be page-locked
-  int pinned_next = 0;
   static constexpr int kGraphs = 16;
   GraphEntry graphs[kGraphs];
   uint64_t tick = 0;
@@ -515,6 +512,7 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   DS4_TRY(h->alloc_t(&h->out_stage, M * d * 4));
   cudaError_t e = ds4::decode_prepare();
   if (e == cudaSuccess) e = ds4::gemm_prepare();
+  if (e == cudaSuccess) e = ds4::router_tc_prepare();
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
@@ -552,18 +550,15 @@ bool is_decode(const ds4moe_handle* h, int n) {
   return n <= ds4::decode_max_tokens() && n * h->s.top_k <= ds4::decode_max_slots();
 }
 
-// Host memory that is page-locked (a graph may copy from and to it); remembered per handle.
-bool host_pinned(ds4moe_handle* h, const void* p) {
-  for (const void* q : h->pinned)
-    if (q == p) return true;
+// Host memory that is page-locked (a graph may copy from and to it). Asked of the driver on every
+// call: a buffer freed and reallocated at the same address may have changed kind.
+bool host_pinned(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  if (at.type != cudaMemoryTypeHost) return false;
-  h->pinned[h->pinned_next++ % ds4moe_handle::kPinned] = p;
-  return true;
+  return at.type == cudaMemoryTypeHost;
 }
 
 extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, const int32_t* token_ids,
@@ -708,8 +703,7 @@ extern "C" int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   DS4_CUDA(cudaStreamIsCapturing(st, &cap));
   if (is_decode(h, n) && h->use_graphs && !h->profile && cap == cudaStreamCaptureStatusNone &&
-      host_pinned(h, x_host) && host_pinned(h, out_host) &&
-      (n_hash == 0 || host_pinned(h, tid_host))) {
+      host_pinned(x_host) && host_pinned(out_host) && (n_hash == 0 || host_pinned(tid_host))) {
     // one graph: host -> device copies, the decode kernels, device -> host copy
     const ds4::DecodeArgs da = decode_args(h, reinterpret_cast<const __nv_bfloat16*>(h->x_stage), n,
                                            n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage);

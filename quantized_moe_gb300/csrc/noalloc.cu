@@ -10,10 +10,11 @@
 // The array (DS4MOE_NOALLOC_MAX_LOGITS floats plus an error word, ~1 MiB) is part of the
 // library image, so every GPU that loads the library holds it until the process exits. Host
 // code cannot use the array's name as a device address; the first call on each device, with
-// that device current, looks the address up with cudaGetSymbolAddress and caches it. Make that
-// first call before any stream capture. Every call on a device shares the one array and leaves
-// the last call's logits in it: calls whose kernels may overlap on the GPU (different streams,
-// no ordering between them) race on it.
+// that device current, looks the address up with cudaGetSymbolAddress and caches it, and raises
+// the router kernel's shared-memory limit in that device's context. Make that first call before
+// any stream capture. Every call on a device shares the one array and leaves the last call's
+// logits in it: calls whose kernels may overlap on the GPU (different streams, no ordering
+// between them) race on it.
 #include <mutex>
 
 #include "../../include/ds4moe.h"
@@ -30,7 +31,8 @@ static __device__ __align__(256) float g_route_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-float* g_scratch_ptr[kMaxDevices] = {};  // device address of g_route_scratch, per device
+float* g_scratch_ptr[kMaxDevices] = {};  // device address of g_route_scratch, per device; set once the
+                                         // device's set-up (address and kernel attribute) succeeded
 
 int scratch_for_current_device(float** out) {
   int dev = -1;
@@ -42,10 +44,15 @@ int scratch_for_current_device(float** out) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess || !p) {
       cudaGetLastError();
       return ds4::set_error(DS4MOE_ERR_CUDA, "ds4moe_route_noalloc: cudaGetSymbolAddress of the static scratch failed");
+    }
+    e = ds4::router_logits_prepare();  // kernel attributes live in each device's context
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return ds4::set_error(DS4MOE_ERR_CUDA, "ds4moe_route_noalloc: setting the router kernel's shared-memory limit failed");
     }
     g_scratch_ptr[dev] = static_cast<float*>(p);
   }
@@ -77,7 +84,8 @@ extern "C" int ds4moe_route_noalloc(const float* router_w, const float* router_b
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* logits = scratch;
   int* err = reinterpret_cast<int*>(scratch + DS4MOE_NOALLOC_MAX_LOGITS);
-  // the error word must start at zero; the logits are fully written before they are read
+  // the top-k kernel's error word starts at zero (only table-routed tokens, which this call does
+  // not route, would set it); the logits are fully written before they are read
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), st);
   if (e == cudaSuccess) {
     ds4::launch_router_logits(static_cast<const __nv_bfloat16*>(x), n_tokens, d, router_w, router_b, n_experts,

@@ -201,13 +201,15 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(const int* __restrict
 void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float* w, const float* b, int n_exp,
                           float* logits, cudaStream_t s) {
   const size_t smem = (size_t)kRouterTok * d * sizeof(__nv_bfloat16);
-  static bool attr_set = false;  // per-process; the attribute is per function, not per device
-  if (!attr_set) {
-    cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set = true;
-  }
   dim3 grid((n_tok + kRouterTok - 1) / kRouterTok, (n_exp + kRouterWarps - 1) / kRouterWarps);
   router_logits_kernel<<<grid, 256, smem, s>>>(x, n_tok, d, w, b, n_exp, logits);
+}
+
+// The kernel stages up to 8 x 12288 bf16 activations (192 KB) in shared memory. Function
+// attributes belong to the current device's context: call once per device before launching there.
+cudaError_t router_logits_prepare() {
+  return cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kRouterTok * 12288 * (int)sizeof(__nv_bfloat16));
 }
 
 void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const int* token_ids, int n_hash,

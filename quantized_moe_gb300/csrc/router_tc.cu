@@ -164,14 +164,23 @@ template <int TT>
 void launch_tt(const __nv_bfloat16* x, int n_tok, int d, const __nv_bfloat16* w3, const float* b, int n_exp,
                float* logits, cudaStream_t s) {
   const dim3 grid((n_tok + TT - 1) / TT, (n_exp + TE - 1) / TE);
-  static bool attr_set = false;  // per process; the attribute belongs to the function
-  if (!attr_set) {
-    cudaFuncSetAttribute(router_tc_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TT>());
-    attr_set = true;
-  }
   router_tc_kernel<TT><<<grid, threads_of<TT>(), smem_bytes<TT>(), s>>>(x, n_tok, d, w3, b, n_exp, logits);
 }
+template <int TT>
+cudaError_t prepare_tt() {
+  return cudaFuncSetAttribute(router_tc_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TT>());
+}
 }  // namespace
+
+// Function attributes belong to the current device's context: called once per device (by the
+// handle's create, with the handle's device current) before any launch there.
+cudaError_t router_tc_prepare() {
+  cudaError_t e = prepare_tt<96>();
+  if (e == cudaSuccess) e = prepare_tt<64>();
+  if (e == cudaSuccess) e = prepare_tt<32>();
+  if (e == cudaSuccess) e = prepare_tt<16>();
+  return e;
+}
 
 // Token tile: the one with the fewest rounds of CTAs over the SMs, weighting a CTA's time by
 // TT + 32 (its weight tile costs about as much as 32 tokens), larger tiles winning ties.
