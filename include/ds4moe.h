@@ -131,6 +131,25 @@ typedef struct ds4moe_handle ds4moe_handle;
  * repacks the weights. Synchronous. On failure *out is set to NULL and nothing leaks. */
 int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out);
 
+/* Expert-parallel partial on one GPU (arc PR #89 "expert parallelism stage 0 + stage 1 (EP=2)",
+ * section "Stage 1 -- EP=2": a rank holds a subset of the routed experts and computes the sum over
+ * its owned slots of w_j E_j(x); the layer output is the plain sum of the ranks' partials).
+ * As ds4moe_create, but the handle holds (copies and repacks) only the routed experts
+ * owned[0..n_owned): distinct ids in [0, n_experts), in any order, read from host memory during
+ * the call; w still describes the full expert stacks. Its forwards route every token over all
+ * n_experts exactly as ds4moe_forward does (the router weights and the hash table are whole), and
+ * write out = the sum over the token's slots whose expert is held of w_j E_j(x), held terms in
+ * ascending expert id, plus S(x) when include_shared is nonzero. With include_shared == 0 the
+ * shared expert is neither copied nor run. The partials of handles whose owned sets partition the
+ * experts, exactly one of them with include_shared, add up to ds4moe_forward's output up to the
+ * fp32 rounding of that sum. ds4moe_get_route returns the whole routing; ds4moe_get_stats counts
+ * only the held experts (counts of the others are 0, distinct_experts counts held experts touched).
+ * Every block format is sliceable by expert (an expert's matrices are whole), so none is refused
+ * here. Errors: DS4MOE_ERR_INVALID_ARG for a NULL owned, n_owned outside 1..n_experts, or an id
+ * out of range or named twice; otherwise as ds4moe_create. */
+int ds4moe_create_subset(const ds4moe_weights* w, const ds4moe_shapes* s, const int32_t* owned, int32_t n_owned,
+                         int32_t include_shared, ds4moe_handle** out);
+
 /* Learned routing for every token. x: device bf16 [n_tokens x d]; out: device fp32
  * [n_tokens x d]; both caller-owned, on the handle's device. stream: a cudaStream_t (NULL =
  * legacy default stream). Asynchronous and stream-ordered: no host synchronisation. A handle

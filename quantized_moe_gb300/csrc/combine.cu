@@ -1,5 +1,6 @@
 // Deterministic combine: out[t] = sum over the token's routed slots, in ascending expert id,
-// of w_j * Y[position of slot j], then + the shared expert's row, all fp32, no atomics.
+// of w_j * Y[position of slot j], then + the shared expert's row, all fp32, no atomics. Slots
+// without a bucketed position (experts the handle does not hold) contribute nothing.
 #include "common.cuh"
 
 namespace ds4 {
@@ -13,6 +14,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ id
                                                       float* __restrict__ out) {
   __shared__ int s_pos[kMaxK];
   __shared__ float s_w[kMaxK];
+  __shared__ int s_n;
   const int t = blockIdx.y;
   if (threadIdx.x == 0) {
     int e[kMaxK], p[kMaxK];
@@ -25,12 +27,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ id
       while (i > 0 && e[i - 1] > ej) { e[i] = e[i - 1]; w[i] = w[i - 1]; p[i] = p[i - 1]; --i; }
       e[i] = ej; w[i] = wj; p[i] = pj;
     }
-    for (int j = 0; j < top_k; ++j) { s_pos[j] = p[j]; s_w[j] = w[j]; }
+    int n = 0;
+    for (int j = 0; j < top_k; ++j)
+      if (p[j] >= 0) {
+        s_pos[n] = p[j];
+        s_w[n++] = w[j];
+      }
+    s_n = n;
   }
   __syncthreads();
   for (int i4 = threadIdx.x * 4; i4 < d; i4 += blockDim.x * 4) {  // the whole row: one sort per token
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < top_k; ++j) {
+    for (int j = 0; j < s_n; ++j) {
       const float4 v = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4));  // read once
       const float w = s_w[j];
       acc.x = fmaf(w, v.x, acc.x);

@@ -144,7 +144,8 @@ struct DecodeArgs {
   int* n_active;
   int* perm;          // [n_tok x top_k]
   int* rowof;
-  int4* work;         // [E] per active expert: expert id, first bucketed position, count (0 past n_active)
+  int4* work;         // [E] per active expert: expert's weight slot, first bucketed position, count (0 past n_active)
+  const int* local_of;  // [E] weight slot of each expert, -1 if the handle does not hold it; null: slot = id
   int* tokof;         // [n_tok x top_k] token of each bucketed position
   float* xscale;      // [n_tok] power-of-two fp16 scale of each token
   int* err;
@@ -208,10 +209,10 @@ int make_act_maps(ActMaps* tm, const void* base, uint64_t rows, uint64_t cols);
 
 // Prefill preparation (see prefill_prep.cu).
 void launch_xprep(const __nv_bfloat16* x, int n_tok, int d, __half* xs16, float* inv_s, cudaStream_t s);
-void launch_gather(const __half* xs16, const float* inv_s, const int* perm, int n_slots, int top_k, int d,
-                   __half* xp16, float* inv_p, cudaStream_t s);
-void launch_tiles(const int* counts, const int* offsets, int n_exp, int tile_n, int4* tiles, int* n_tiles,
-                  cudaStream_t s);
+void launch_gather(const __half* xs16, const float* inv_s, const int* perm, const int* n_pos, int n_slots, int top_k,
+                   int d, __half* xp16, float* inv_p, cudaStream_t s);
+void launch_tiles(const int* counts, const int* offsets, int n_exp, const int* local_of, int tile_n, int4* tiles,
+                  int* n_tiles, cudaStream_t s);
 
 void launch_repack(int fmt, const uint8_t* src, uint8_t* dst, int total_rows, int k, cudaStream_t s);
 void launch_q2k_dmax(const uint8_t* packed, size_t bytes, unsigned* out, cudaStream_t s);
@@ -225,9 +226,11 @@ void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float*
 void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const int* token_ids, int n_hash,
                  const int* table, int vocab, int* idx, float* wts, int* err, cudaStream_t s);
 int bucket_chunks(int n_slots);  // ints of the bucketing scratch: bucket_chunks(n_slots) * n_exp
-void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* ghist, cudaStream_t s);
-void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, int* counts, int* offsets,
-                           int* active, int* n_active, int* perm, int* rowof, cudaStream_t s);
+// local_of: [n_exp] weight slot of each expert, -1 for experts the handle does not hold (their slots
+// are left out of the bucketing); null when the handle holds every expert.
+void launch_bucket_count(const int* idx, int n_slots, int n_exp, const int* local_of, int* ghist, cudaStream_t s);
+void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, const int* local_of, int* counts,
+                           int* offsets, int* active, int* n_active, int* perm, int* rowof, cudaStream_t s);
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s);
 

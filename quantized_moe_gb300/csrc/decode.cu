@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
     // lower index: the order of the warp selection below), and the k winners are bucketed in
     // closed form (one position each, in ascending expert id).
     __shared__ float s_sc[256], s_selw[16];
-    __shared__ int s_sel[16];
+    __shared__ int s_sel[16], s_loc[16];
     const int ex = threadIdx.x;
     const float sc = ex < E ? 1.f / (1.f + expf(-__ldcg(a.logits + ex))) : -1.f;
     s_sc[ex] = sc;
@@ -117,32 +117,45 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
       if (rank < K) {
         s_sel[rank] = ex;
         s_selw[rank] = sc;
+        s_loc[rank] = a.local_of ? a.local_of[ex] : ex;  // < 0: an expert this handle does not hold
       }
     }
     __syncthreads();
+    // the selected experts this handle holds take one bucketed position each, in ascending id
+    int n_own = 0;
+    for (int q = 0; q < K; ++q) n_own += s_loc[q] >= 0;
     if (threadIdx.x < K) {
       const int r = threadIdx.x, er = s_sel[r];
       float sum = 0.f;
       for (int q = 0; q < K; ++q) sum += s_selw[q];  // selection order, as the warp version
       int pos = 0;
-      for (int q = 0; q < K; ++q) pos += s_sel[q] < er;
+      for (int q = 0; q < K; ++q) pos += s_sel[q] < er && s_loc[q] >= 0;
       a.idx[r] = er;
       a.wts[r] = s_selw[r] / sum;
-      a.perm[pos] = r;
-      a.rowof[r] = pos;
-      a.tokof[pos] = 0;
-      a.active[pos] = er;
-      a.work[pos] = make_int4(er, pos, 1, 1);
+      if (s_loc[r] >= 0) {
+        a.perm[pos] = r;
+        a.rowof[r] = pos;
+        a.tokof[pos] = 0;
+        a.active[pos] = er;
+        a.work[pos] = make_int4(s_loc[r], pos, 1, 1);
+      } else {
+        a.rowof[r] = -1;
+      }
+      if (r >= n_own) a.work[r] = make_int4(0, 0, 0, 0);  // the work list ends at n_own
     }
     if (ex < E) {
       int off = 0;
-      for (int q = 0; q < K; ++q) off += s_sel[q] < ex;
-      a.counts[ex] = rank < K ? 1 : 0;
+      bool own = false;
+      for (int q = 0; q < K; ++q) {
+        off += s_sel[q] < ex && s_loc[q] >= 0;
+        own |= s_sel[q] == ex && s_loc[q] >= 0;
+      }
+      a.counts[ex] = own ? 1 : 0;
       a.offsets[ex] = off;
     }
     if (threadIdx.x == 0) {
-      a.offsets[E] = K;
-      *a.n_active = K;
+      a.offsets[E] = n_own;
+      *a.n_active = n_own;
     }
     for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
     if (threadIdx.x == 0) *a.counter = 0u;
@@ -194,7 +207,8 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   }
   for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = 0;
   __syncthreads();
-  for (int sl = threadIdx.x; sl < n_slots; sl += kThreads) atomicAdd(&s_cnt[s_idx[sl]], 1);  // integer counts
+  for (int sl = threadIdx.x; sl < n_slots; sl += kThreads)  // integer counts of the experts held
+    if (!a.local_of || a.local_of[s_idx[sl]] >= 0) atomicAdd(&s_cnt[s_idx[sl]], 1);
   __syncthreads();
   if (warp == 0) {  // exclusive scans of the counts and of the active flags (E <= 256: 8 per lane)
     int c[8];
@@ -231,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
     int4 w = make_int4(0, 0, 0, 0);
     if (i < s_nact) {
       const int ex = s_act[i];
-      w = make_int4(ex, s_off[ex], s_cnt[ex], 0);
+      w = make_int4(a.local_of ? a.local_of[ex] : ex, s_off[ex], s_cnt[ex], 0);
       a.active[i] = ex;
     }
     a.work[i] = w;
@@ -242,6 +256,10 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   }
   for (int sl = threadIdx.x; sl < n_slots; sl += kThreads) {  // stable rank among equal experts
     const int ex = s_idx[sl];
+    if (a.local_of && a.local_of[ex] < 0) {  // not held: no bucketed position, no term
+      a.rowof[sl] = -1;
+      continue;
+    }
     int r = 0;
     for (int j = 0; j < sl; ++j) r += s_idx[j] == ex;
     const int pos = s_off[ex] + r;
@@ -745,6 +763,7 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int
     }
     float o = 0.f;
     for (int j = 0; j < K; ++j) {
+      if (ps[j] < 0) continue;  // an expert this handle does not hold
       float y = 0.f;
       for (int w = 0; w < kWarps; ++w) y += part0[((size_t)w * n_slots + ps[j]) * 16 + r];
       o = fmaf(wv[j], y, o);

@@ -80,6 +80,10 @@ struct ds4moe_handle {
   uint8_t* sdown = nullptr;
   int* table = nullptr;
   size_t mb_gu = 0, mb_d = 0, mb_sgu = 0, mb_sd = 0;
+  // expert subset (ds4moe_create_subset): weight slot of each expert, -1 where not held; null when
+  // the handle holds every expert
+  int* local_of = nullptr;
+  int n_local = 0;  // experts held (weight slots)
   // workspace
   float* logits = nullptr;
   int* idx = nullptr;
@@ -311,14 +315,20 @@ int copy_in(void* dst, const void* src, size_t bytes, int device, const char* wh
   return DS4MOE_OK;
 }
 
-// Repacks n_mat canonical [rows x k] matrices (back to back) into dst.
+// Repacks n_mat canonical [rows x k] matrices into dst (back to back): matrices mats[0..n_mat) of
+// the source stack, or its first n_mat when mats is null.
 int repack_stack(ds4moe_handle* h, int fmt, const void* src, uint8_t* dst, int n_mat, int rows, int k,
-                 const char* what) {
+                 const char* what, const int* mats = nullptr) {
   const size_t mb = ds4::matrix_bytes(fmt, rows, k);
   const PtrKind kind = classify(src, h->s.device);
   if (kind == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than %d", what, h->s.device);
+  const uint8_t* src8 = static_cast<const uint8_t*>(src);
   if (kind == PTR_DEVICE) {
-    ds4::launch_repack(fmt, static_cast<const uint8_t*>(src), dst, n_mat * rows, k, 0);
+    if (!mats) {
+      ds4::launch_repack(fmt, src8, dst, n_mat * rows, k, 0);
+    } else {
+      for (int m = 0; m < n_mat; ++m) ds4::launch_repack(fmt, src8 + mb * mats[m], dst + mb * m, rows, k, 0);
+    }
     DS4_CUDA(cudaGetLastError());
     DS4_CUDA(cudaDeviceSynchronize());
     return DS4MOE_OK;
@@ -335,7 +345,13 @@ int repack_stack(ds4moe_handle* h, int fmt, const void* src, uint8_t* dst, int n
   int rc = DS4MOE_OK;
   for (int m0 = 0; m0 < n_mat && rc == DS4MOE_OK; m0 += per) {
     const int n = std::min(per, n_mat - m0);
-    e = cudaMemcpy(stage, static_cast<const uint8_t*>(src) + mb * m0, mb * n, cudaMemcpyHostToDevice);
+    if (!mats) {
+      e = cudaMemcpy(stage, src8 + mb * m0, mb * n, cudaMemcpyHostToDevice);
+    } else {
+      e = cudaSuccess;
+      for (int m = 0; m < n && e == cudaSuccess; ++m)
+        e = cudaMemcpy(stage + mb * m, src8 + mb * mats[m0 + m], mb, cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) {
       ds4::launch_repack(fmt, stage, dst + mb * m0, n * rows, k, 0);
       e = cudaGetLastError();
@@ -369,10 +385,10 @@ int check_q2k_scales(ds4moe_handle* h) {
   const uint8_t* stacks[4] = {nullptr, nullptr, nullptr, nullptr};
   size_t bytes[4] = {0, 0, 0, 0};
   if (s.fmt_gate_up == DS4MOE_FMT_Q2_K) {
-    stacks[0] = h->gate; bytes[0] = h->mb_gu * s.n_experts;
-    stacks[1] = h->up; bytes[1] = h->mb_gu * s.n_experts;
+    stacks[0] = h->gate; bytes[0] = h->mb_gu * h->n_local;
+    stacks[1] = h->up; bytes[1] = h->mb_gu * h->n_local;
   }
-  if (s.fmt_down == DS4MOE_FMT_Q2_K) { stacks[2] = h->down; bytes[2] = h->mb_d * s.n_experts; }
+  if (s.fmt_down == DS4MOE_FMT_Q2_K) { stacks[2] = h->down; bytes[2] = h->mb_d * h->n_local; }
   unsigned* dmax = nullptr;
   DS4_CUDA(cudaMalloc(&dmax, 4));
   cudaError_t e = cudaMemset(dmax, 0, 4);
@@ -410,12 +426,35 @@ int check_q2k_scales(ds4moe_handle* h) {
 
 }  // namespace
 
-extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out) {
+// owned: host list of the experts the handle holds (null: all); include_shared: keep the shared expert.
+static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const int32_t* owned, int n_owned,
+                int include_shared, ds4moe_handle** out) {
   if (!out) return fail(DS4MOE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (!w || !s) return fail(DS4MOE_ERR_INVALID_ARG, "weights or shapes is NULL");
-  int rc = check_shapes(s);
+  if (!w || !s_in) return fail(DS4MOE_ERR_INVALID_ARG, "weights or shapes is NULL");
+  int rc = check_shapes(s_in);
   if (rc != DS4MOE_OK) return rc;
+  ds4moe_shapes shp = *s_in;
+  const ds4moe_shapes* s = &shp;
+  std::vector<int> held;  // the experts held, ascending; local slot = position in this list
+  std::vector<int> local_of;
+  if (owned) {
+    if (n_owned < 1 || n_owned > s->n_experts)
+      return fail(DS4MOE_ERR_INVALID_ARG, "n_owned=%d must be in 1..n_experts=%d", n_owned, s->n_experts);
+    local_of.assign(s->n_experts, -1);
+    for (int i = 0; i < n_owned; ++i) {
+      const int e = owned[i];
+      if (e < 0 || e >= s->n_experts) return fail(DS4MOE_ERR_INVALID_ARG, "owned[%d]=%d is outside [0, n_experts=%d)", i, e, s->n_experts);
+      if (local_of[e] != -1) return fail(DS4MOE_ERR_INVALID_ARG, "owned names expert %d twice", e);
+      local_of[e] = 0;
+    }
+    for (int e = 0; e < s->n_experts; ++e)
+      if (local_of[e] == 0) {
+        local_of[e] = (int)held.size();
+        held.push_back(e);
+      }
+    if (!include_shared) shp.n_shared = 0;  // this handle's partial leaves the shared expert out
+  }
   if (!w->router_w || !w->gate || !w->up || !w->down) return fail(DS4MOE_ERR_INVALID_ARG, "router_w, gate, up and down are required");
   if (s->has_bias && !w->router_b) return fail(DS4MOE_ERR_INVALID_ARG, "has_bias set but router_b is NULL");
   if (s->n_shared && (!w->shared_gate || !w->shared_up || !w->shared_down))
@@ -432,6 +471,9 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   const int E = s->n_experts, d = s->d, f = s->f_routed, fs = s->f_shared, K = s->top_k;
   h->mb_gu = ds4::matrix_bytes(s->fmt_gate_up, f, d);
   h->mb_d = ds4::matrix_bytes(s->fmt_down, d, f);
+  h->n_local = owned ? (int)held.size() : E;
+  const int L = h->n_local;
+  const int* mats = owned ? held.data() : nullptr;
   // weights
   DS4_TRY(h->alloc_t(&h->router_w, (size_t)E * d * 4));
   DS4_TRY(copy_in(h->router_w, w->router_w, (size_t)E * d * 4, s->device, "router_w"));
@@ -439,12 +481,16 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
     DS4_TRY(h->alloc_t(&h->router_b, (size_t)E * 4));
     DS4_TRY(copy_in(h->router_b, w->router_b, (size_t)E * 4, s->device, "router_b"));
   }
-  DS4_TRY(h->alloc_t(&h->gate, h->mb_gu * E));
-  DS4_TRY(h->alloc_t(&h->up, h->mb_gu * E));
-  DS4_TRY(h->alloc_t(&h->down, h->mb_d * E));
-  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->gate, h->gate, E, f, d, "gate"));
-  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->up, h->up, E, f, d, "up"));
-  DS4_TRY(repack_stack(h, s->fmt_down, w->down, h->down, E, d, f, "down"));
+  DS4_TRY(h->alloc_t(&h->gate, h->mb_gu * L));
+  DS4_TRY(h->alloc_t(&h->up, h->mb_gu * L));
+  DS4_TRY(h->alloc_t(&h->down, h->mb_d * L));
+  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->gate, h->gate, L, f, d, "gate", mats));
+  DS4_TRY(repack_stack(h, s->fmt_gate_up, w->up, h->up, L, f, d, "up", mats));
+  DS4_TRY(repack_stack(h, s->fmt_down, w->down, h->down, L, d, f, "down", mats));
+  if (owned) {
+    DS4_TRY(h->alloc_t(&h->local_of, (size_t)E * 4));
+    DS4_TRY(copy_in(h->local_of, local_of.data(), (size_t)E * 4, s->device, "expert map"));
+  }
   if (s->n_shared) {
     h->mb_sgu = ds4::matrix_bytes(s->fmt_shared, fs, d);
     h->mb_sd = ds4::matrix_bytes(s->fmt_shared, d, fs);
@@ -529,8 +575,21 @@ extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds
   return DS4MOE_OK;
 }
 
+extern "C" int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out) {
+  return create_impl(w, s, nullptr, 0, 1, out);
+}
+
+extern "C" int ds4moe_create_subset(const ds4moe_weights* w, const ds4moe_shapes* s, const int32_t* owned,
+                                    int32_t n_owned, int32_t include_shared, ds4moe_handle** out) {
+  if (!owned) {
+    if (out) *out = nullptr;
+    return fail(DS4MOE_ERR_INVALID_ARG, "owned is NULL");
+  }
+  return create_impl(w, s, owned, n_owned, include_shared, out);
+}
+
 // Arguments of the decode kernels for one forward over the handle's workspace.
-ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, int n, const int32_t* token_ids, int n_hash,
+static ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, int n, const int32_t* token_ids, int n_hash,
                             float* out) {
   const ds4moe_shapes& s = h->s;
   ds4::DecodeArgs da{};
@@ -543,16 +602,17 @@ ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, int n, co
   da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = s.f_routed;
   da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
   da.fs = s.f_shared; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
+  da.local_of = h->local_of;
   return da;
 }
 
-bool is_decode(const ds4moe_handle* h, int n) {
+static bool is_decode(const ds4moe_handle* h, int n) {
   return n <= ds4::decode_max_tokens() && n * h->s.top_k <= ds4::decode_max_slots();
 }
 
 // Host memory that is page-locked (a graph may copy from and to it). Asked of the driver on every
 // call: a buffer freed and reallocated at the same address may have changed kind.
-bool host_pinned(const void* p) {
+static bool host_pinned(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
@@ -632,18 +692,18 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
   ds4::launch_topk(h->logits, n_learned, E, K, token_ids, n_hash, h->table, s.hash_vocab, h->idx, h->wts, h->err, st);
   mark("topk");
-  ds4::launch_bucket_count(h->idx, n * K, E, h->ghist, st);
+  ds4::launch_bucket_count(h->idx, n * K, E, h->local_of, h->ghist, st);
   mark("bucket_count");
-  ds4::launch_bucket_scatter(h->idx, n * K, E, h->ghist, h->counts, h->offsets, h->active, h->n_active, h->perm,
-                             h->rowof, st);
+  ds4::launch_bucket_scatter(h->idx, n * K, E, h->ghist, h->local_of, h->counts, h->offsets, h->active, h->n_active,
+                             h->perm, h->rowof, st);
   mark("bucket_scatter");
   if (!h->has_prefill) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d needs the batched path, not sized at create", n);
   ds4::launch_xprep(xb, n, d, h->Xs16, h->inv_s, st);
   mark("xprep");
-  ds4::launch_gather(h->Xs16, h->inv_s, h->perm, n * K, K, d, h->Xp16, h->inv_p, st);
+  ds4::launch_gather(h->Xs16, h->inv_s, h->perm, h->offsets + E, n * K, K, d, h->Xp16, h->inv_p, st);
   mark("gather");
   const int TN = routed_tile_n(s);  // one tiling serves the gate/up and the down GEMM
-  ds4::launch_tiles(h->counts, h->offsets, E, TN, h->tiles, h->n_tiles, st);
+  ds4::launch_tiles(h->counts, h->offsets, E, h->local_of, TN, h->tiles, h->n_tiles, st);
   mark("tiles");
   const int routed_tiles = (n * K + TN - 1) / TN + std::min(E, n * K), dense_tiles = (n + TN - 1) / TN;
   ds4::GemmArgs g{};

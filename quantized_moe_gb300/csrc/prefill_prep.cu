@@ -45,12 +45,14 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
 }
 
 // One warp per bucketed position: copy the token's fp16 row; each lane issues eight 16-byte loads
-// before its stores, so a warp keeps 4 KB in flight.
+// before its stores, so a warp keeps 4 KB in flight. The bucketed positions end at *n_pos (every
+// slot, or the slots of the experts the handle holds).
 __global__ void __launch_bounds__(256) gather_kernel(const __half* __restrict__ xs16, const float* __restrict__ inv_s,
-                                                     const int* __restrict__ perm, int n_slots, int top_k, int d,
-                                                     __half* __restrict__ xp16, float* __restrict__ inv_p) {
+                                                     const int* __restrict__ perm, const int* __restrict__ n_pos,
+                                                     int n_slots, int top_k, int d, __half* __restrict__ xp16,
+                                                     float* __restrict__ inv_p) {
   const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (pos >= n_slots) return;
+  if (pos >= n_slots || pos >= *n_pos) return;
   const int tok = perm[pos] / top_k;
   const uint4* src = reinterpret_cast<const uint4*>(xs16 + (size_t)tok * d);
   uint4* dst = reinterpret_cast<uint4*>(xp16 + (size_t)pos * d);
@@ -72,9 +74,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const __half* __restrict__ 
 }
 
 // One thread per expert: ceil(count / tile_n) tiles, placed by an exclusive scan over experts.
+// The tile's first field is the expert's weight slot (local_of[e], or e when every expert is held).
 __global__ void __launch_bounds__(256) tiles_kernel(const int* __restrict__ counts, const int* __restrict__ offsets,
-                                                    int n_exp, int tile_n, int4* __restrict__ tiles,
-                                                    int* __restrict__ n_tiles) {
+                                                    int n_exp, const int* __restrict__ local_of, int tile_n,
+                                                    int4* __restrict__ tiles, int* __restrict__ n_tiles) {
   __shared__ int wsum[8];
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
   const int cnt = e < n_exp ? counts[e] : 0;
@@ -94,7 +97,8 @@ __global__ void __launch_bounds__(256) tiles_kernel(const int* __restrict__ coun
   }
   const int first = base + inc - nt;
   const int off = e < n_exp ? offsets[e] : 0;
-  for (int j = 0; j < nt; ++j) tiles[first + j] = make_int4(e, off + j * tile_n, min(tile_n, cnt - j * tile_n), 0);
+  const int slot = (e < n_exp && local_of) ? local_of[e] : e;
+  for (int j = 0; j < nt; ++j) tiles[first + j] = make_int4(slot, off + j * tile_n, min(tile_n, cnt - j * tile_n), 0);
   if (e == 0) *n_tiles = total;
 }
 
@@ -104,14 +108,14 @@ void launch_xprep(const __nv_bfloat16* x, int n_tok, int d, __half* xs16, float*
   xprep_kernel<<<n_tok, 256, 0, s>>>(x, d, xs16, inv_s);
 }
 
-void launch_gather(const __half* xs16, const float* inv_s, const int* perm, int n_slots, int top_k, int d,
-                   __half* xp16, float* inv_p, cudaStream_t s) {
-  gather_kernel<<<(n_slots + 7) / 8, 256, 0, s>>>(xs16, inv_s, perm, n_slots, top_k, d, xp16, inv_p);
+void launch_gather(const __half* xs16, const float* inv_s, const int* perm, const int* n_pos, int n_slots, int top_k,
+                   int d, __half* xp16, float* inv_p, cudaStream_t s) {
+  gather_kernel<<<(n_slots + 7) / 8, 256, 0, s>>>(xs16, inv_s, perm, n_pos, n_slots, top_k, d, xp16, inv_p);
 }
 
-void launch_tiles(const int* counts, const int* offsets, int n_exp, int tile_n, int4* tiles, int* n_tiles,
-                  cudaStream_t s) {
-  tiles_kernel<<<1, 256, 0, s>>>(counts, offsets, n_exp, tile_n, tiles, n_tiles);
+void launch_tiles(const int* counts, const int* offsets, int n_exp, const int* local_of, int tile_n, int4* tiles,
+                  int* n_tiles, cudaStream_t s) {
+  tiles_kernel<<<1, 256, 0, s>>>(counts, offsets, n_exp, local_of, tile_n, tiles, n_tiles);
 }
 
 }  // namespace ds4

@@ -111,12 +111,15 @@ constexpr int kChunk = 1024;
 
 // Pass 1: per-chunk histogram of the experts (integer counts, order-free).
 __global__ void __launch_bounds__(256) bucket_hist_kernel(const int* __restrict__ idx, int n_slots, int n_exp,
-                                                          int* __restrict__ ghist) {
+                                                          const int* __restrict__ local_of, int* __restrict__ ghist) {
   __shared__ int hist[256];
   if (threadIdx.x < n_exp) hist[threadIdx.x] = 0;
   __syncthreads();
   const int s0 = blockIdx.x * kChunk;
-  for (int i = threadIdx.x; i < kChunk && s0 + i < n_slots; i += 256) atomicAdd(&hist[idx[s0 + i]], 1);
+  for (int i = threadIdx.x; i < kChunk && s0 + i < n_slots; i += 256) {
+    const int e = idx[s0 + i];
+    if (!local_of || local_of[e] >= 0) atomicAdd(&hist[e], 1);  // only the experts this handle holds
+  }
   __syncthreads();
   if (threadIdx.x < n_exp) ghist[(size_t)blockIdx.x * n_exp + threadIdx.x] = hist[threadIdx.x];
 }
@@ -124,9 +127,11 @@ __global__ void __launch_bounds__(256) bucket_hist_kernel(const int* __restrict_
 // Pass 2: chunk b places its slots at offsets[e] + (slots of e in earlier chunks) + (earlier slots
 // of e in this chunk), so positions are sorted by (expert, slot) = (expert, token, slot). Ranks
 // inside a round of 256 slots come from warp match masks and per-warp counts. Chunk 0 also
-// publishes counts, offsets, the active experts and their number.
+// publishes counts, offsets, the active experts and their number. Slots of experts the handle does
+// not hold get no position (rowof = -1).
 __global__ void __launch_bounds__(256) bucket_place_kernel(const int* __restrict__ idx, int n_slots, int n_exp,
                                                            const int* __restrict__ ghist, int n_chunks,
+                                                           const int* __restrict__ local_of,
                                                            int* __restrict__ counts, int* __restrict__ offsets,
                                                            int* __restrict__ active, int* __restrict__ n_active,
                                                            int* __restrict__ perm, int* __restrict__ rowof) {
@@ -175,7 +180,11 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(const int* __restrict
     for (int k = threadIdx.x; k < 8 * 256; k += 256) (&wcnt[0][0])[k] = 0;
     __syncthreads();
     const int sl = s0 + r0 + threadIdx.x;
-    const int ex = sl < n_slots ? idx[sl] : -1;
+    int ex = sl < n_slots ? idx[sl] : -1;
+    if (ex >= 0 && local_of && local_of[ex] < 0) {
+      rowof[sl] = -1;
+      ex = -1;
+    }
     const unsigned m = __match_any_sync(0xffffffffu, ex);
     const int rank = __popc(m & lt);
     if (ex >= 0 && rank == 0) wcnt[warp][ex] = __popc(m);
@@ -222,15 +231,15 @@ void launch_topk(const float* logits, int n_learned, int n_exp, int top_k, const
 
 int bucket_chunks(int n_slots) { return (n_slots + kChunk - 1) / kChunk; }
 
-void launch_bucket_count(const int* idx, int n_slots, int n_exp, int* ghist, cudaStream_t s) {
-  bucket_hist_kernel<<<bucket_chunks(n_slots), 256, 0, s>>>(idx, n_slots, n_exp, ghist);
+void launch_bucket_count(const int* idx, int n_slots, int n_exp, const int* local_of, int* ghist, cudaStream_t s) {
+  bucket_hist_kernel<<<bucket_chunks(n_slots), 256, 0, s>>>(idx, n_slots, n_exp, local_of, ghist);
 }
 
-void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, int* counts, int* offsets,
-                           int* active, int* n_active, int* perm, int* rowof, cudaStream_t s) {
+void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, const int* local_of, int* counts,
+                           int* offsets, int* active, int* n_active, int* perm, int* rowof, cudaStream_t s) {
   const int nc = bucket_chunks(n_slots);
-  bucket_place_kernel<<<nc, 256, 0, s>>>(idx, n_slots, n_exp, ghist, nc, counts, offsets, active, n_active, perm,
-                                         rowof);
+  bucket_place_kernel<<<nc, 256, 0, s>>>(idx, n_slots, n_exp, ghist, nc, local_of, counts, offsets, active, n_active,
+                                         perm, rowof);
 }
 
 }  // namespace ds4

@@ -28,7 +28,7 @@ DS4MOE_FMT_Q8_0 = 0
 DS4MOE_FMT_Q2_K = 1
 FORMATS = {"q8_0": DS4MOE_FMT_Q8_0, "q2_k": DS4MOE_FMT_Q2_K}
 
-EXPORTED = ("ds4moe_create", "ds4moe_forward", "ds4moe_forward_ex", "ds4moe_forward_host",
+EXPORTED = ("ds4moe_create", "ds4moe_create_subset", "ds4moe_forward", "ds4moe_forward_ex", "ds4moe_forward_host",
             "ds4moe_get_route", "ds4moe_get_stats", "ds4moe_device_bytes",
             "ds4moe_launches_per_forward", "ds4moe_set_profiling", "ds4moe_get_phase_times", "ds4moe_route_noalloc",
             "ds4moe_destroy", "ds4moe_last_error")
@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         L.ds4moe_create.argtypes = [ctypes.POINTER(ds4moe_weights), ctypes.POINTER(ds4moe_shapes), ctypes.POINTER(vp)]
         L.ds4moe_create.restype = ctypes.c_int
+        L.ds4moe_create_subset.argtypes = [ctypes.POINTER(ds4moe_weights), ctypes.POINTER(ds4moe_shapes), vp, i32,
+                                           i32, ctypes.POINTER(vp)]
+        L.ds4moe_create_subset.restype = ctypes.c_int
         L.ds4moe_forward.argtypes = [vp, vp, i32, vp, vp]
         L.ds4moe_forward.restype = ctypes.c_int
         L.ds4moe_forward_ex.argtypes = [vp, vp, i32, vp, i32, vp, vp]
@@ -140,6 +143,16 @@ def make_weights(router_w, router_b, gate, up, down, shared_gate=None, shared_up
 def ds4moe_create(weights: ds4moe_weights, shapes: ds4moe_shapes) -> int:
     h = ctypes.c_void_p()
     _check(lib().ds4moe_create(ctypes.byref(weights), ctypes.byref(shapes), ctypes.byref(h)))
+    return h.value
+
+
+def ds4moe_create_subset(weights: ds4moe_weights, shapes: ds4moe_shapes, owned, include_shared: bool) -> int:
+    """A handle holding only the routed experts in `owned` (see the header); returns its address."""
+    ids = np.ascontiguousarray(np.asarray(owned, dtype=np.int32).reshape(-1))
+    buf = ids if ids.size else np.zeros(1, np.int32)  # a valid address even for an empty list
+    h = ctypes.c_void_p()
+    _check(lib().ds4moe_create_subset(ctypes.byref(weights), ctypes.byref(shapes), buf.ctypes.data, int(ids.size),
+                                      int(bool(include_shared)), ctypes.byref(h)))
     return h.value
 
 

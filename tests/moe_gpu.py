@@ -8,7 +8,9 @@ import synthetic
 from quantized_moe_gb300 import ds4moe as api
 
 
-def create(p: synthetic.Problem, max_tokens: int | None = None, device: int = 0, workspace_limit: int = 0):
+def create(p: synthetic.Problem, max_tokens: int | None = None, device: int = 0, workspace_limit: int = 0,
+           owned=None, include_shared: bool = True):
+    """A handle for the problem; with `owned`, one holding only those routed experts."""
     s = p.spec
     shapes = api.make_shapes(s.d, s.f, s.f_shared, s.n_experts, s.top_k, s.n_shared, s.fmt_gate_up, s.fmt_down,
                              s.fmt_shared, p.router_b is not None, s.hash_vocab,
@@ -18,6 +20,8 @@ def create(p: synthetic.Problem, max_tokens: int | None = None, device: int = 0,
             p.shared_gate, p.shared_up, p.shared_down, p.hash_table]
     keep = [None if a is None else np.ascontiguousarray(a) for a in keep]
     weights = api.make_weights(*keep)
+    if owned is not None:
+        return api.ds4moe_create_subset(weights, shapes, owned, include_shared)
     return api.ds4moe_create(weights, shapes)
 
 

@@ -69,3 +69,26 @@ def test_create_requires_shared_tensors_and_bias(api):
     with pytest.raises(api.Ds4MoeError) as ei:
         api.ds4moe_create(api.make_weights(w, None, w, w, w, w, w, w), _shapes(api, has_bias=True))
     assert ei.value.code == api.DS4MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("owned,msg", [([], "n_owned"), (list(range(9)), "n_owned"), ([0, 8], "outside"),
+                                       ([-1], "outside"), ([3, 1, 3], "twice")])
+def test_create_subset_rejects_bad_expert_lists_on_host(api, owned, msg):
+    """An expert subset names 1..n_experts distinct ids in range; refused before any device work."""
+    w = np.zeros(16, np.float32)
+    weights = api.make_weights(w, None, w, w, w, w, w, w)
+    with pytest.raises(api.Ds4MoeError) as ei:
+        api.ds4moe_create_subset(weights, _shapes(api), owned, True)
+    assert ei.value.code == api.DS4MOE_ERR_INVALID_ARG
+    assert msg in api.ds4moe_last_error()
+
+
+def test_create_subset_null_list(api):
+    lib = api.lib()
+    w = np.zeros(16, np.float32)
+    weights = api.make_weights(w, None, w, w, w, w, w, w)
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.ds4moe_create_subset(ctypes.byref(weights), ctypes.byref(_shapes(api)), None, 2, 1,
+                                    ctypes.byref(h)) == api.DS4MOE_ERR_INVALID_ARG
+    assert "owned is NULL" in api.ds4moe_last_error()
