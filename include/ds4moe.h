@@ -215,6 +215,18 @@ int ds4moe_get_phase_times(ds4moe_handle* h, float* ms, const char** names, int3
 int ds4moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int32_t n_tokens,
                          int32_t d, int32_t n_experts, int32_t top_k, int32_t* idx, float* w, void* stream);
 
+/* Test hook of the failure path (no counterpart in the paper: it exists so that the bounded waits
+ * of the batched expert GEMM can be shown to end with an error status instead of a hang). The next
+ * batched forward of h (more than 16 tokens, or more than 128 routed slots) runs its routed
+ * gate/up GEMM with every pipeline wait limited to about 1 ms instead of about 1 s, and the first
+ * CTA of that launch withholds one dequant arrival of its K stage `stage` (counted over the CTA's
+ * work items). That stage never becomes full, so the MMA's wait for it runs out: the CTA stops,
+ * lets its issued copies and MMAs finish, frees its tensor memory and records error bit 2 plus a
+ * bit naming the wait (see ds4moe_stats.error_flags); that forward's output is incomplete. The
+ * hook applies to one forward and then clears itself. stage >= 0; DS4MOE_ERR_INVALID_ARG
+ * otherwise. */
+int ds4moe_set_test_stall(ds4moe_handle* h, int32_t stage);
+
 /* Frees everything the handle owns. NULL is allowed. Synchronises the device first. */
 void ds4moe_destroy(ds4moe_handle* h);
 

@@ -193,6 +193,9 @@ struct GemmArgs {
   float* y_out;            // down output [row][ld_out] fp32
   int ld_out;
   int* err;                // error bits: 4 = a pipeline wait timed out, 8 = |h| beyond fp16 range
+  long long timeout_cycles;  // limit of every pipeline wait in SM cycles; 0: the default (~1 s)
+  int test_stall;          // 0; or s + 1: the first CTA withholds one dequant arrival of its K stage s (tests
+                           // of the timeout path: the MMA's wait for that stage runs out)
 };
 
 // Largest token tile the expert GEMM takes for a weight format (FMT_*).

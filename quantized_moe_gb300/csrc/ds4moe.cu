@@ -134,6 +134,8 @@ struct ds4moe_handle {
   cudaEvent_t ev[kMaxPhases + 1] = {};
   const char* phase_name[kMaxPhases] = {};
   int n_phases = 0;
+  // test of the GEMM timeout path (ds4moe_set_test_stall): stage + 1 for the next batched forward
+  int test_stall = 0;
 
   // Decode forwards replay a captured CUDA graph of their three launches (launching each kernel
   // from the host costs far more than a graph node). Graphs are keyed by the call's token
@@ -709,6 +711,11 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   ds4::GemmArgs g{};
   g.w0 = h->gate; g.w1 = h->up; g.mat_bytes = h->mb_gu; g.k = d; g.tiles = h->tiles; g.n_tiles = h->n_tiles;
   g.inv_scale = h->inv_p; g.h_out = h->H16; g.ld_out = f; g.err = h->err;
+  if (h->test_stall) {  // one-shot: withhold one arrival, waits give up after ~1 ms (2e6 cycles)
+    g.test_stall = h->test_stall;
+    g.timeout_cycles = 2000000;
+    h->test_stall = 0;
+  }
   cudaError_t ge = ds4::launch_gemm(s.fmt_gate_up, true, h->tm_xp, g, f / 64, routed_tiles, st);
   if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(ge));
   mark("routed_gateup");
@@ -824,6 +831,13 @@ extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n
   // router, top-k, 2 bucketing, activation prep + gather, tile list, routed gate/up and down GEMMs,
   // the same for the shared expert, combine
   return 1 + 1 + 2 + 2 + 1 + 2 + (h->s.n_shared ? 2 : 0) + 1;
+}
+
+extern "C" int ds4moe_set_test_stall(ds4moe_handle* h, int32_t stage) {
+  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (stage < 0) return fail(DS4MOE_ERR_INVALID_ARG, "stage=%d is negative", stage);
+  h->test_stall = stage + 1;
+  return DS4MOE_OK;
 }
 
 extern "C" int ds4moe_set_profiling(ds4moe_handle* h, int32_t enable) {

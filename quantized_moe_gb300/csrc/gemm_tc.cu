@@ -181,17 +181,19 @@ __device__ __forceinline__ void deq_q2k_stage(const uint32_t (&unit)[NR], int su
     deq_q2k_quad<4, NR>(w, sc01, sc23, rc, a_base, aoff);
 }
 
-// Waits (bounded, without raising errors) for a phase: used only to let copies land before exit.
-__device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity) {
+// Waits (bounded, without raising errors) for a phase: used only to let copies land, or issued MMAs
+// finish, before the CTA exits.
+__device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();
-  while (!mbar_try(bar, parity) && clock64() - t0 < kTimeoutCycles) {
+  while (!mbar_try(bar, parity) && clock64() - t0 < limit) {
   }
 }
 
 // mbar_wait by lane 0 of a converged warp, its result given to every lane.
-__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site) {
+__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site,
+                                           long long limit) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err, site);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err, site, limit);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -275,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   const int n_items = item_count<C::BN>(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
   const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
+  const long long limit = p.timeout_cycles > 0 ? p.timeout_cycles : kTimeoutCycles;
 
   Bars b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         const int rg0 = GATEUP ? 4 * t.mt : 8 * t.mt;  // first 16-row group of the slice
         for (int uN = 0; uN < n_kb; ++uN, ++gu) {
           const int rs = gu % RAWS;
-          if (!mbar_wait(&b.raw_empty[rs], ((gu / RAWS) & 1) ^ 1, abort_flag, p.err, 1)) break;
+          if (!mbar_wait(&b.raw_empty[rs], ((gu / RAWS) & 1) ^ 1, abort_flag, p.err, 1, limit)) break;
           unsigned char* dst = smem + C::OFF_RAW + rs * C::RAW_BYTES;
           mbar_expect_tx(&b.raw_full[rs], GATEUP ? 2 * raw_copy : raw_copy);
           bulk_load(dst, src0 + unit_offset(rg0, uN, n_kb, UB), raw_copy, &b.raw_full[rs]);
@@ -334,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
       }
       // the last copies land before the CTA may exit (after an abort they may still be in flight)
-      for (uint32_t k = gu > (uint32_t)RAWS ? gu - RAWS : 0; k < gu; ++k) bounded_try(&b.raw_full[k % RAWS], (k / RAWS) & 1);
+      for (uint32_t k = gu > (uint32_t)RAWS ? gu - RAWS : 0; k < gu; ++k)
+        bounded_try(&b.raw_full[k % RAWS], (k / RAWS) & 1, limit);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ activation producer
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         const Item t = item_of<C::BN>(p, it);
         for (int sB = 0; sB < n_stages; ++sB, ++gs) {
           const int sb = gs % STAGES;
-          if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2)) break;
+          if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
           const int rows = t.nbox * BOX_ROWS;  // rows fetched: 128-row boxes, then a 64-row one
           mbar_expect_tx(&b.full[sb], rows * BK * 2);
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
       }
       for (uint32_t k = gs > (uint32_t)STAGES ? gs - STAGES : 0; k < gs; ++k)
-        bounded_try(&b.full[k % STAGES], (k / STAGES) & 1);
+        bounded_try(&b.full[k % STAGES], (k / STAGES) & 1, limit);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -366,14 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       const Item t = item_of<C::BN>(p, it);
       const int buf = local & 1;
       // the epilogue has drained this buffer (item local - 2)
-      if (!lane0_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6)) break;
+      if (!lane0_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6, limit)) break;
       tc_fence_after();
       const uint32_t idesc = idesc_f16_f32(BM, t.n);
       const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS);
       bool ok = true;
       for (int s = 0; s < n_stages; ++s, ++gs) {
         const int st = gs % STAGES;
-        if (!lane0_wait(&b.full[st], (gs / STAGES) & 1, abort_flag, p.err, 7)) {
+        if (!lane0_wait(&b.full[st], (gs / STAGES) & 1, abort_flag, p.err, 7, limit)) {
           ok = false;
           break;
         }
@@ -388,6 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       if (!ok) break;
       tc_commit_elect(&b.acc_full[buf]);
     }
+    // After an abort, the MMAs already issued must finish before TMEM is freed: the commit of the
+    // last issued stage (stage gs - 1) arrives only once all of them have completed.
+    if (*abort_flag && gs > 0 && lane == 0) bounded_try(&b.empty[(gs - 1) % STAGES], ((gs - 1) / STAGES) & 1, limit);
+    __syncwarp();
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
     // NG groups of warps take K stages round-robin, NG = the stages per raw unit (Q2_K four, Q8_0
@@ -410,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         // the raw units follow the stages: unit gs / kpu of the CTA's sequence (kpu == NG)
         const uint32_t gu = gs / kpu;
         const int rs = gu % RAWS, sa = gs % STAGES, su = gs % kpu;
-        if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3)) { ok = false; break; }
-        if (!mbar_wait(&b.empty[sa], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 4)) { ok = false; break; }
+        if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3, limit)) { ok = false; break; }
+        if (!mbar_wait(&b.empty[sa], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
         const uint32_t raw = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES);
         const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
         if constexpr (FMT == FMT_Q2_K) {
@@ -430,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&b.full[sa]);
+          // (a test of the timeout path withholds one arrival: that stage never becomes full)
+          if (!(p.test_stall && blockIdx.x == 0 && gs + 1 == (uint32_t)p.test_stall)) mbar_arrive(&b.full[sa]);
           mbar_arrive(&b.raw_empty[rs]);  // the group's only stage of this unit is done
         }
       }
@@ -445,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       const Item t = item_of<C::BN>(p, it);
       const int buf = local & 1;
       // all four warps enter the item's epilogue (it has named barriers) only together
-      if (!named_bar_all(1, 32 * kEpiWarps, mbar_wait(&b.acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 5)))
+      if (!named_bar_all(1, 32 * kEpiWarps, mbar_wait(&b.acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 5, limit)))
         break;
       tc_fence_after();
       if (GATEUP) {  // the tile's activation scales, once per item

@@ -10,7 +10,8 @@ namespace ds4 {
 namespace tc {
 
 // A wait that has not completed after this many SM cycles (about a second) is abandoned: the
-// kernel records an error bit and stops instead of spinning forever.
+// kernel records an error bit and stops instead of spinning forever. (A launch may set a shorter
+// limit: see GemmArgs::timeout_cycles.)
 constexpr long long kTimeoutCycles = 2000000000ll;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -50,12 +51,12 @@ __device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity) {
 // bit 2 of *err and bit 16 + site, which names the wait that gave up) if it does not complete in
 // time, or if another thread already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int site = 0) {
+                                          int site = 0, long long limit = kTimeoutCycles) {
   if (mbar_try(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_sleep(b, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(err, 4 | (1 << (16 + site)));
       return false;

@@ -31,6 +31,7 @@ FORMATS = {"q8_0": DS4MOE_FMT_Q8_0, "q2_k": DS4MOE_FMT_Q2_K}
 EXPORTED = ("ds4moe_create", "ds4moe_create_subset", "ds4moe_forward", "ds4moe_forward_ex", "ds4moe_forward_host",
             "ds4moe_get_route", "ds4moe_get_stats", "ds4moe_device_bytes",
             "ds4moe_launches_per_forward", "ds4moe_set_profiling", "ds4moe_get_phase_times", "ds4moe_route_noalloc",
+            "ds4moe_set_test_stall",
             "ds4moe_destroy", "ds4moe_last_error")
 DS4MOE_NOALLOC_MAX_LOGITS = 262144
 
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.ds4moe_get_phase_times.restype = ctypes.c_int
         L.ds4moe_route_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.ds4moe_route_noalloc.restype = ctypes.c_int
+        L.ds4moe_set_test_stall.argtypes = [vp, i32]
+        L.ds4moe_set_test_stall.restype = ctypes.c_int
         L.ds4moe_destroy.argtypes = [vp]
         L.ds4moe_destroy.restype = None
         L.ds4moe_last_error.argtypes = []
@@ -209,6 +212,11 @@ def ds4moe_route_noalloc(router_w, router_b, x, n_tokens: int, d: int, n_experts
     """Routing without any device allocation (for callers that cannot allocate); see the header."""
     _check(lib().ds4moe_route_noalloc(_ptr(router_w), _ptr(router_b), _ptr(x), n_tokens, d, n_experts, top_k,
                                       _ptr(idx), _ptr(w), stream))
+
+
+def ds4moe_set_test_stall(h: int, stage: int) -> None:
+    """Test hook: the next batched forward's GEMM withholds one arrival and its waits give up (see the header)."""
+    _check(lib().ds4moe_set_test_stall(h, stage))
 
 
 def ds4moe_destroy(h: Optional[int]) -> None:
