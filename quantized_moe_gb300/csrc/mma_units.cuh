@@ -86,15 +86,30 @@ __device__ __forceinline__ XFrag xfrag_f32(const float* __restrict__ chunk, floa
   return f;
 }
 
-// Lane masks for the B operand: all ones in MMA i for the lanes of group g == i.
+// Lane selectors for the B operand, as fp16x2 multipliers: 1.0 in MMA i for the lanes of group
+// g == i, 0 otherwise. The selection is an fp16 multiply (FMA pipe) rather than an AND: the integer
+// pipe already carries the quant field extraction. (x * 1.0 is x exactly; x * 0 is a signed zero.)
+#ifndef DS4_BSEL_AND
+#define DS4_BSEL_AND 0
+#endif
 struct BMask {
   uint32_t m[8];
   __device__ __forceinline__ BMask() {
     const int g = (threadIdx.x & 31) >> 2;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = (g == i) ? 0xffffffffu : 0u;
+    for (int i = 0; i < 8; ++i) m[i] = (g == i) ? (DS4_BSEL_AND ? 0xffffffffu : 0x3C003C00u) : 0u;
   }
 };
+
+__device__ __forceinline__ uint32_t bsel(uint32_t b, uint32_t sel) {
+#if DS4_BSEL_AND
+  return b & sel;
+#else
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(b), "r"(sel));
+  return r;
+#endif
+}
 
 // Exact small-integer extraction through an fp32 with exponent 2^23: (bits | 0x4B000000) is
 // 2^23 + field * 2^pos, and fmaf(v, c, -2^23 c) gives field * 2^pos * c exactly.
@@ -155,14 +170,14 @@ __device__ __forceinline__ void q2k_chunk_mma(const uint32_t (&w)[4], const uint
   float e[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two shorter dependency chains
   d[0] = d[1] = d[2] = d[3] = 0.f;
   uint32_t a[4];
-  q2k_a<0>(w, wh, a); mma_f16_16816(d, a, x.b0 & bm.m[0], x.b1 & bm.m[0]);
-  q2k_a<1>(w, wh, a); mma_f16_16816(e, a, x.b0 & bm.m[1], x.b1 & bm.m[1]);
-  q2k_a<2>(w, wh, a); mma_f16_16816(d, a, x.b0 & bm.m[2], x.b1 & bm.m[2]);
-  q2k_a<3>(w, wh, a); mma_f16_16816(e, a, x.b0 & bm.m[3], x.b1 & bm.m[3]);
-  q2k_a<4>(w, wh, a); mma_f16_16816(d, a, x.b0 & bm.m[4], x.b1 & bm.m[4]);
-  q2k_a<5>(w, wh, a); mma_f16_16816(e, a, x.b0 & bm.m[5], x.b1 & bm.m[5]);
-  q2k_a<6>(w, wh, a); mma_f16_16816(d, a, x.b0 & bm.m[6], x.b1 & bm.m[6]);
-  q2k_a<7>(w, wh, a); mma_f16_16816(e, a, x.b0 & bm.m[7], x.b1 & bm.m[7]);
+  q2k_a<0>(w, wh, a); mma_f16_16816(d, a, bsel(x.b0, bm.m[0]), bsel(x.b1, bm.m[0]));
+  q2k_a<1>(w, wh, a); mma_f16_16816(e, a, bsel(x.b0, bm.m[1]), bsel(x.b1, bm.m[1]));
+  q2k_a<2>(w, wh, a); mma_f16_16816(d, a, bsel(x.b0, bm.m[2]), bsel(x.b1, bm.m[2]));
+  q2k_a<3>(w, wh, a); mma_f16_16816(e, a, bsel(x.b0, bm.m[3]), bsel(x.b1, bm.m[3]));
+  q2k_a<4>(w, wh, a); mma_f16_16816(d, a, bsel(x.b0, bm.m[4]), bsel(x.b1, bm.m[4]));
+  q2k_a<5>(w, wh, a); mma_f16_16816(e, a, bsel(x.b0, bm.m[5]), bsel(x.b1, bm.m[5]));
+  q2k_a<6>(w, wh, a); mma_f16_16816(d, a, bsel(x.b0, bm.m[6]), bsel(x.b1, bm.m[6]));
+  q2k_a<7>(w, wh, a); mma_f16_16816(e, a, bsel(x.b0, bm.m[7]), bsel(x.b1, bm.m[7]));
   // columns are disjoint between the two accumulators' contributions except for zeros
   d[0] += e[0]; d[1] += e[1]; d[2] += e[2]; d[3] += e[3];
 }
@@ -179,9 +194,9 @@ __device__ __forceinline__ void q80_chunk_mma(const uint4 (&v)[4], const BMask& 
     const uint32_t a[4] = {prmt(wa, 0u, 0x4140u), prmt(wa, 0u, 0x4342u), prmt(wb, 0u, 0x4140u),
                            prmt(wb, 0u, 0x4342u)};
     if (i & 1)
-      mma_f16_16816(e, a, x.b0 & bm.m[i], x.b1 & bm.m[i]);
+      mma_f16_16816(e, a, bsel(x.b0, bm.m[i]), bsel(x.b1, bm.m[i]));
     else
-      mma_f16_16816(d, a, x.b0 & bm.m[i], x.b1 & bm.m[i]);
+      mma_f16_16816(d, a, bsel(x.b0, bm.m[i]), bsel(x.b1, bm.m[i]));
   }
   d[0] += e[0]; d[1] += e[1]; d[2] += e[2]; d[3] += e[3];
 }
