@@ -150,7 +150,8 @@ struct DecodeArgs {
   float* xscale;      // [n_tok] power-of-two fp16 scale of each token
   int* err;
   unsigned int* counter;  // arrival counter of the route kernel, zero between forwards
-  float* hmax;        // [n_tok x top_k + n_tok] max |h| per routed slot position, then per token
+  float* hmax;        // [n_tok x top_k] max |h| per routed slot position
+  float* hsg;         // [n_tok][fs / 16] max |h| of the shared expert per token and 16-row group
   const uint8_t* gate;
   const uint8_t* up;
   const uint8_t* down;

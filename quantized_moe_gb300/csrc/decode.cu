@@ -5,19 +5,21 @@
 //                         the last CTA to finish (atomic arrival counter, no waiting) runs the
 //                         sigmoid top-k (or table routing), the bucketing, and publishes a work
 //                         list (expert, first position, count) per active expert, the token of
-//                         every bucketed position and the fp16 scale of every token.
-//  gateup_decode_kernel   CTA = 16 rows of f of one active expert (or of the shared expert), K
-//                         split over 8 warps, each warp streaming its units through a two-deep
-//                         register pipeline; h = silu(g) * u in fp32 plus max|h| per row of H
-//                         (integer atomicMax: order-free).
+//                         every bucketed position and the fp16 scale of every token. Further CTAs
+//                         (one per 16 rows of f_shared) compute the shared expert's gate/up, which
+//                         needs no routing, alongside the router.
+//  gateup_decode_kernel   CTA = 16 rows of f of one active expert, K split over 8 warps, each warp
+//                         streaming its units through a two-deep register pipeline; h = silu(g) * u
+//                         in fp32 plus max|h| per row of H (integer atomicMax: order-free).
 //  down_decode_kernel     CTA = 16 rows of d for every touched expert and the shared expert;
 //                         (expert, K unit) items are dealt round-robin to the warps, each warp
 //                         accumulates its partials in shared memory in a fixed order, and the
 //                         CTA writes the final rows: routed terms in ascending expert id, then
 //                         the shared expert.
 //
-// Weights that do not depend on the previous kernel's output are loaded before waiting on it:
-// the shared expert's gate/up units, and (the routing being final by then) every down unit.
+// Tokens are processed one per pass (an expert with several tokens streams its weight units once
+// per token, the later passes from L2). Weights that do not depend on the previous kernel's output
+// are loaded before waiting on it: every down unit (the routing being final by then).
 #include "mma_units.cuh"
 
 namespace ds4 {
@@ -28,10 +30,25 @@ constexpr int kThreads = 256;
 constexpr int kMaxTok = 16;
 constexpr int kMaxSlots = 128;
 constexpr int kMaxJ = 12;  // d <= 12288: float4 loads per lane of one router row slice
+// Tokens per pass of the GEMV kernels. One: every pass streams the item's weight units again (the
+// later passes from L2), and the kernels fit in 128 registers, so two CTAs (16 warps) run per SM.
+// Passes of two tokens needed up to 254 registers (one CTA per SM) and measured slower on batched
+// decode (16 tokens: 753 against 608 us per forward).
+constexpr int kPass = 1;
 
 // ----------------------------------------------------------------------------- route
 
-__global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
+template <int FMT_S>
+__device__ void shared_gateup_cta(const DecodeArgs& a, int rg);
+
+template <int FMT_S>
+__global__ void __launch_bounds__(kThreads, 2) route_decode_kernel(DecodeArgs a) {
+  // CTAs past the routed experts compute the shared expert's gate/up, which needs no routing: it
+  // overlaps the router and its serial top-k tail instead of following them.
+  if ((int)blockIdx.x >= a.n_exp) {
+    shared_gateup_cta<FMT_S>(a, blockIdx.x - a.n_exp);
+    return;
+  }
   __shared__ float part[kWarps][kMaxTok];
   __shared__ float xmx[kWarps][kMaxTok];
   __shared__ int s_last;
@@ -91,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
   if (threadIdx.x == 0) {
     unsigned prev;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.counter) : "memory");
-    s_last = prev == gridDim.x - 1;
+    s_last = prev == (unsigned)a.n_exp - 1;  // the router CTAs only
   }
   __syncthreads();
   if (!s_last) return;
@@ -157,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
       a.offsets[E] = n_own;
       *a.n_active = n_own;
     }
-    for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
+    for (int i = threadIdx.x; i < n_slots; i += kThreads) a.hmax[i] = 0.f;
     if (threadIdx.x == 0) *a.counter = 0u;
     return;
   }
@@ -267,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) route_decode_kernel(DecodeArgs a) {
     a.rowof[sl] = pos;
     a.tokof[pos] = sl / K;
   }
-  for (int i = threadIdx.x; i < n_slots + nt; i += kThreads) a.hmax[i] = 0.f;
+  for (int i = threadIdx.x; i < n_slots; i += kThreads) a.hmax[i] = 0.f;
   if (threadIdx.x == 0) *a.counter = 0u;  // every CTA has arrived: ready for the next forward
 }
 
@@ -410,11 +427,13 @@ __device__ __forceinline__ void gu_stream(GuStage<FMT, P>& s0, GuStage<FMT, P>& 
   }
 }
 
-// Quad and warp reductions of one pass, SwiGLU, store of h and of max|h| per row.
-template <int P>
+// Quad and warp reductions of one pass, SwiGLU, store of h and of max|h| over the 16 rows: into
+// hmax[row0 + tt] with an integer atomicMax (order-free), or, with GROUP_MAX, as a plain store into
+// hmax[(row0 + tt) * n_groups + rg] (one entry per row group, reduced by the reader).
+template <int P, bool GROUP_MAX = false>
 __device__ __forceinline__ void gu_epilogue(float (&red)[kWarps][2][P][16], const float (&accg)[P][2],
                                             const float (&accu)[P][2], const float (&sc)[P], int np, float* hbase,
-                                            int ldh, int row0, int rg, float* hmax_row0) {
+                                            int ldh, int row0, int rg, float* hmax, int n_groups = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int tt = 0; tt < P; ++tt)
@@ -439,46 +458,22 @@ __device__ __forceinline__ void gu_epilogue(float (&red)[kWarps][2][P][16], cons
     float m = fabsf(h);
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, 16));
-    if (valid && r == 0) atomicMax(reinterpret_cast<unsigned*>(hmax_row0 + tt), __float_as_uint(m));
+    if (valid && r == 0) {
+      if (GROUP_MAX)
+        hmax[(size_t)(row0 + tt) * n_groups + rg] = m;
+      else
+        atomicMax(reinterpret_cast<unsigned*>(hmax + row0 + tt), __float_as_uint(m));
+    }
   }
   __syncthreads();
 }
 
-template <int FMT_R, int FMT_S, int P>
-__global__ void __launch_bounds__(kThreads) gateup_decode_kernel(DecodeArgs a, int max_active) {
+template <int FMT_R, int P>
+__global__ void __launch_bounds__(kThreads, 2) gateup_decode_kernel(DecodeArgs a, int max_active) {
   __shared__ float red[kWarps][2][P][16];
   const int rg = blockIdx.x, warp = threadIdx.x >> 5;
-  const bool shared = (int)blockIdx.y == max_active;
   const BMask bm;
   const Q2kLaneConst qc;
-  if (shared) {
-    if (rg * 16 >= a.fs) return;
-    const int n_kb = a.d / unit_k(FMT_S);
-    GuStage<FMT_S, P> s0, s1;
-    const int nk = n_kb > warp ? (n_kb - warp + kWarps - 1) / kWarps : 0;
-    // the shared expert does not depend on the routing: load its first units right away
-    if (nk > 0) gu_load_w(s0, a.sgate, a.sup, rg, warp, n_kb);
-    if (nk > 1) gu_load_w(s1, a.sgate, a.sup, rg, warp + kWarps, n_kb);
-    pdl_wait();
-    pdl_trigger();
-    for (int p0 = 0; p0 < a.n_tok; p0 += P) {
-      const int np = min(P, a.n_tok - p0);
-      const __nv_bfloat16* xrow[P];
-      float sc[P];
-#pragma unroll
-      for (int tt = 0; tt < P; ++tt) {
-        const int tok = p0 + min(tt, np - 1);
-        xrow[tt] = a.x + (size_t)tok * a.d;
-        sc[tt] = a.xscale[tok];
-      }
-      float accg[P][2], accu[P][2];
-#pragma unroll
-      for (int tt = 0; tt < P; ++tt) accg[tt][0] = accg[tt][1] = accu[tt][0] = accu[tt][1] = 0.f;
-      gu_stream<FMT_S, P>(s0, s1, p0 == 0, a.sgate, a.sup, rg, n_kb, xrow, sc, np, bm, qc, accg, accu);
-      gu_epilogue<P>(red, accg, accu, sc, np, a.Hs, a.fs, p0, rg, a.hmax + a.n_tok * a.top_k + p0);
-    }
-    return;
-  }
   if (rg * 16 >= a.f) return;
   pdl_wait();
   pdl_trigger();
@@ -503,7 +498,61 @@ __global__ void __launch_bounds__(kThreads) gateup_decode_kernel(DecodeArgs a, i
 #pragma unroll
     for (int tt = 0; tt < P; ++tt) accg[tt][0] = accg[tt][1] = accu[tt][0] = accu[tt][1] = 0.f;
     gu_stream<FMT_R, P>(s0, s1, false, w0, w1, rg, n_kb, xrow, sc, np, bm, qc, accg, accu);
-    gu_epilogue<P>(red, accg, accu, sc, np, a.H, a.f, pos0 + p0, rg, a.hmax + pos0 + p0);
+    gu_epilogue<P>(red, accg, accu, sc, np, a.H, a.f, pos0 + p0, rg, a.hmax);
+  }
+}
+
+// The shared expert's gate/up for 16 rows (row group rg of f_shared) and every token, run by the
+// route kernel's extra CTAs. The token scales are computed here (the router's CTA 0 publishes
+// them only for the routed kernels); max|h| of the 16 rows goes to hsg[token][rg] (the down
+// kernel reduces over the row groups).
+template <int FMT_S>
+__device__ void shared_gateup_cta(const DecodeArgs& a, int rg) {
+  constexpr int P = kPass;
+  __shared__ float red[kWarps][2][P][16];
+  __shared__ float s_xsc[kMaxTok];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (rg * 16 >= a.fs) return;
+  const BMask bm;
+  const Q2kLaneConst qc;
+  const int n_kb = a.d / unit_k(FMT_S);
+  GuStage<FMT_S, P> s0, s1;
+  const int nk = n_kb > warp ? (n_kb - warp + kWarps - 1) / kWarps : 0;
+  // the first units are in flight while the token scales are computed
+  if (nk > 0) gu_load_w(s0, a.sgate, a.sup, rg, warp, n_kb);
+  if (nk > 1) gu_load_w(s1, a.sgate, a.sup, rg, warp + kWarps, n_kb);
+  for (int t = warp; t < a.n_tok; t += kWarps) {
+    const __nv_bfloat16* xr = a.x + (size_t)t * a.d;
+    float m = 0.f;
+    for (int k = lane * 8; k < a.d; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    m = warp_max(m);
+    if (lane == 0) s_xsc[t] = fp16_row_scale(m);
+  }
+  __syncthreads();
+  const int n_groups = a.fs / 16;
+  for (int p0 = 0; p0 < a.n_tok; p0 += P) {
+    const int np = min(P, a.n_tok - p0);
+    const __nv_bfloat16* xrow[P];
+    float sc[P];
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) {
+      const int tok = p0 + min(tt, np - 1);
+      xrow[tt] = a.x + (size_t)tok * a.d;
+      sc[tt] = s_xsc[tok];
+    }
+    float accg[P][2], accu[P][2];
+#pragma unroll
+    for (int tt = 0; tt < P; ++tt) accg[tt][0] = accg[tt][1] = accu[tt][0] = accu[tt][1] = 0.f;
+    gu_stream<FMT_S, P>(s0, s1, p0 == 0, a.sgate, a.sup, rg, n_kb, xrow, sc, np, bm, qc, accg, accu);
+    gu_epilogue<P, true>(red, accg, accu, sc, np, a.Hs, a.fs, p0, rg, a.hsg, n_groups);
   }
 }
 
@@ -542,17 +591,22 @@ struct HPre {
   float hm[P];
 };
 
+// max|h| of row `row` of the item's h: routed slots from the gate/up kernel's atomic maxima, the
+// shared expert's tokens from the CTA's shared-memory copy (s_hms).
+__device__ __forceinline__ float item_hmax(const DecodeArgs& a, const DownItem& it, int row, const float* s_hms) {
+  return it.shared ? s_hms[row] : __ldcg(a.hmax + row);
+}
+
 template <int FMT, int P>
-__device__ __forceinline__ void h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp) {
+__device__ __forceinline__ void h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp, const float* s_hms) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* hbase = it.shared ? a.Hs : a.H;
-  const float* hmax = it.shared ? a.hmax + a.n_tok * a.top_k : a.hmax;
   const int kdim = it.shared ? a.fs : a.f;
 #pragma unroll
   for (int tt = 0; tt < P; ++tt) {
     if (tt >= it.cnt) break;
     const int row = it.pos0 + tt;
-    hp.hm[tt] = __ldcg(hmax + row);
+    hp.hm[tt] = item_hmax(a, it, row, s_hms);
 #pragma unroll
     for (int c = 0; c < Unit<FMT>::kChunks; ++c) {
       const float* base = hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c;
@@ -579,10 +633,9 @@ __device__ __forceinline__ XFrag xfrag_vals(float2 v0, float2 v1, float sc) {
 template <int FMT, int P>
 __device__ __forceinline__ void down_item_compute(const DecodeArgs& a, const DownItem& it, const Unit<FMT>& u,
                                                   const HPre<P>& hp, float* part_rows, const BMask& bm,
-                                                  const Q2kLaneConst& qc, int kdim) {
+                                                  const Q2kLaneConst& qc, int kdim, const float* s_hms) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* hbase = it.shared ? a.Hs : a.H;
-  const float* hmax = it.shared ? a.hmax + a.n_tok * a.top_k : a.hmax;
   for (int p0 = 0; p0 < it.cnt; p0 += P) {
     const int np = min(P, it.cnt - p0);
     float sc[P];
@@ -596,7 +649,7 @@ __device__ __forceinline__ void down_item_compute(const DecodeArgs& a, const Dow
 #pragma unroll
         for (int c = 0; c < Unit<FMT>::kChunks; ++c) xf[tt][c] = xfrag_vals(hp.v[tt][c][0], hp.v[tt][c][1], sc[tt]);
       } else {
-        sc[tt] = fp16_row_scale(__ldcg(hmax + row));
+        sc[tt] = fp16_row_scale(item_hmax(a, it, row, s_hms));
 #pragma unroll
         for (int c = 0; c < Unit<FMT>::kChunks; ++c)
           xf[tt][c] = xfrag_f32(hbase + (size_t)row * kdim + it.kb * unit_k(FMT) + 128 * c, sc[tt]);
@@ -681,23 +734,24 @@ __device__ __forceinline__ void down_load(const DownItem& it, RawUnit& b, int rg
 template <int FMT_R, int FMT_S, int P>
 __device__ __forceinline__ void down_item_run(const DecodeArgs& a, const DownItem& it, const RawUnit& b,
                                               const HPre<P>& hp, float* part, float* parts, const BMask& bm,
-                                              const Q2kLaneConst& qc) {
+                                              const Q2kLaneConst& qc, const float* s_hms) {
   if (it.shared)
-    down_item_compute<FMT_S, P>(a, it, as_unit<FMT_S>(b), hp, parts, bm, qc, a.fs);
+    down_item_compute<FMT_S, P>(a, it, as_unit<FMT_S>(b), hp, parts, bm, qc, a.fs, s_hms);
   else
-    down_item_compute<FMT_R, P>(a, it, as_unit<FMT_R>(b), hp, part, bm, qc, a.f);
+    down_item_compute<FMT_R, P>(a, it, as_unit<FMT_R>(b), hp, part, bm, qc, a.f, s_hms);
 }
 
 template <int FMT_R, int FMT_S, int P>
-__device__ __forceinline__ void down_h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp) {
+__device__ __forceinline__ void down_h_prefetch(const DecodeArgs& a, const DownItem& it, HPre<P>& hp,
+                                                const float* s_hms) {
   if (it.shared)
-    h_prefetch<FMT_S, P>(a, it, hp);
+    h_prefetch<FMT_S, P>(a, it, hp, s_hms);
   else
-    h_prefetch<FMT_R, P>(a, it, hp);
+    h_prefetch<FMT_R, P>(a, it, hp, s_hms);
 }
 
 template <int FMT_R, int FMT_S, int P>
-__global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int max_active) {
+__global__ void __launch_bounds__(kThreads, 2) down_decode_kernel(DecodeArgs a, int max_active) {
   extern __shared__ __align__(16) float dsm[];
   const int rg = blockIdx.x, warp = threadIdx.x >> 5;
   const int nt = a.n_tok, K = a.top_k, n_slots = nt * K;
@@ -724,23 +778,35 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(DecodeArgs a, int
     down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
   }
   pdl_wait();
+  // max|h| of each token of the shared expert, over the per-row-group maxima of its gate/up CTAs
+  __shared__ float s_hms[kMaxTok];
+  if (a.n_shared) {
+    const int n_groups = a.fs / 16, lane = threadIdx.x & 31;
+    for (int t = warp; t < nt; t += kWarps) {
+      float m = 0.f;
+      for (int j = lane; j < n_groups; j += 32) m = fmaxf(m, __ldcg(a.hsg + (size_t)t * n_groups + j));
+      m = warp_max(m);
+      if (lane == 0) s_hms[t] = m;
+    }
+  }
+  __syncthreads();
   // h of the two preloaded items (H is complete now); later items fetch theirs with their units
   HPre<P> h0, h1;
-  if (warp < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0);
-  if (warp + kWarps < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1);
+  if (warp < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0, s_hms);
+  if (warp + kWarps < n_items) down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1, s_hms);
   for (int i = warp; i < n_items; i += 2 * kWarps) {
-    down_item_run<FMT_R, FMT_S, P>(a, it0, b0, h0, part, parts, bm, qc);
+    down_item_run<FMT_R, FMT_S, P>(a, it0, b0, h0, part, parts, bm, qc, s_hms);
     if (i + 2 * kWarps < n_items) {
       it0 = down_item(a, i + 2 * kWarps, n_routed, n_kb_r);
       down_load<FMT_R, FMT_S>(it0, b0, rg, n_kb_r, n_kb_s);
-      down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0);
+      down_h_prefetch<FMT_R, FMT_S, P>(a, it0, h0, s_hms);
     }
     if (i + kWarps < n_items) {
-      down_item_run<FMT_R, FMT_S, P>(a, it1, b1, h1, part, parts, bm, qc);
+      down_item_run<FMT_R, FMT_S, P>(a, it1, b1, h1, part, parts, bm, qc, s_hms);
       if (i + 3 * kWarps < n_items) {
         it1 = down_item(a, i + 3 * kWarps, n_routed, n_kb_r);
         down_load<FMT_R, FMT_S>(it1, b1, rg, n_kb_r, n_kb_s);
-        down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1);
+        down_h_prefetch<FMT_R, FMT_S, P>(a, it1, h1, s_hms);
       }
     }
   }
@@ -793,10 +859,9 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, size_t smem, cudaStream_t s, bool 
   return cudaLaunchKernelEx(&cfg, kernel, a, max_active);
 }
 
-template <int R, int S>
+template <int R>
 cudaError_t launch_gu(dim3 grid, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
-  return a.n_tok == 1 ? launch_ex(gateup_decode_kernel<R, S, 1>, grid, 0, s, pdl, a, max_active)
-                      : launch_ex(gateup_decode_kernel<R, S, 2>, grid, 0, s, pdl, a, max_active);
+  return launch_ex(gateup_decode_kernel<R, kPass>, grid, 0, s, pdl, a, max_active);
 }
 
 template <int R, int S, int P>
@@ -806,16 +871,12 @@ cudaError_t launch_dn_p(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const 
 
 template <int R, int S>
 cudaError_t prepare_dn() {
-  cudaError_t e = cudaFuncSetAttribute(down_decode_kernel<R, S, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(down_decode_kernel<R, S, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-  return e;
+  return cudaFuncSetAttribute(down_decode_kernel<R, S, kPass>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
 }
 
 template <int R, int S>
 cudaError_t launch_dn(dim3 grid, size_t smem, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
-  return a.n_tok == 1 ? launch_dn_p<R, S, 1>(grid, smem, s, pdl, a, max_active)
-                      : launch_dn_p<R, S, 2>(grid, smem, s, pdl, a, max_active);
+  return launch_dn_p<R, S, kPass>(grid, smem, s, pdl, a, max_active);
 }
 
 }  // namespace
@@ -834,16 +895,18 @@ int decode_max_slots() { return kMaxSlots; }
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks) {
   const int max_active = min(a.n_exp, a.n_tok * a.top_k);
-  route_decode_kernel<<<a.n_exp, kThreads, 0, s>>>(a);
+  // the routed experts' router CTAs, then the shared expert's gate/up CTAs (one per 16 rows)
+  const int route_grid = a.n_exp + (a.n_shared ? a.fs / 16 : 0);
+  if (a.n_shared && fmt_s == FMT_Q2_K)
+    route_decode_kernel<FMT_Q2_K><<<route_grid, kThreads, 0, s>>>(a);
+  else
+    route_decode_kernel<FMT_Q8_0><<<route_grid, kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "route");
-  const dim3 g_gu(max(a.f, a.n_shared ? a.fs : 0) / 16, max_active + (a.n_shared ? 1 : 0));
-  const int fsg = a.n_shared ? fmt_s : fmt_r_gu;
-  if (fmt_r_gu == FMT_Q2_K && fsg == FMT_Q2_K) e = launch_gu<FMT_Q2_K, FMT_Q2_K>(g_gu, s, pdl, a, max_active);
-  else if (fmt_r_gu == FMT_Q2_K) e = launch_gu<FMT_Q2_K, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
-  else if (fsg == FMT_Q2_K) e = launch_gu<FMT_Q8_0, FMT_Q2_K>(g_gu, s, pdl, a, max_active);
-  else e = launch_gu<FMT_Q8_0, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
+  const dim3 g_gu(a.f / 16, max_active);
+  e = fmt_r_gu == FMT_Q2_K ? launch_gu<FMT_Q2_K>(g_gu, s, pdl, a, max_active)
+                           : launch_gu<FMT_Q8_0>(g_gu, s, pdl, a, max_active);
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "gateup");
   const int fsd = a.n_shared ? fmt_s : fmt_r_d;

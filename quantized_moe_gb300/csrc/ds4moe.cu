@@ -97,6 +97,7 @@ struct ds4moe_handle {
   int* ghist = nullptr;  // batched bucketing: per-chunk expert histograms
   float* H = nullptr;   // decode: h per routed slot, fp32
   float* Hs = nullptr;  // decode: h of the shared expert, fp32
+  float* hsg = nullptr;  // decode: max |h| of the shared expert per token and 16-row group
   float* Y = nullptr;   // prefill: down output per bucketed slot, fp32
   float* Ys = nullptr;  // prefill: shared expert output per token, fp32
   // prefill tensor-core path
@@ -522,7 +523,10 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
   DS4_TRY(h->alloc_t(&h->ghist, (size_t)ds4::bucket_chunks((int)slots) * E * 4));
   const size_t Md = std::min<size_t>(M, (size_t)ds4::decode_max_tokens());  // decode buffers
   DS4_TRY(h->alloc_t(&h->H, Md * K * f * 4));
-  if (s->n_shared) DS4_TRY(h->alloc_t(&h->Hs, Md * fs * 4));
+  if (s->n_shared) {
+    DS4_TRY(h->alloc_t(&h->Hs, Md * fs * 4));
+    DS4_TRY(h->alloc_t(&h->hsg, Md * (size_t)(fs / 16) * 4));
+  }
   h->has_prefill = M > (size_t)ds4::decode_max_tokens() || slots > (size_t)ds4::decode_max_slots();
   if (h->has_prefill) {
     DS4_TRY(h->alloc_t(&h->Y, slots * d * 4));
@@ -603,7 +607,7 @@ static ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, in
   da.work = h->work; da.tokof = h->tokof; da.xscale = h->xscale;
   da.gate = h->gate; da.up = h->up; da.down = h->down; da.mb_gu = h->mb_gu; da.mb_d = h->mb_d; da.f = s.f_routed;
   da.sgate = h->sgate; da.sup = h->sup; da.sdown = h->sdown; da.mb_sgu = h->mb_sgu; da.mb_sd = h->mb_sd;
-  da.fs = s.f_shared; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.out = out;
+  da.fs = s.f_shared; da.n_shared = s.n_shared; da.H = h->H; da.Hs = h->Hs; da.hsg = h->hsg; da.out = out;
   da.local_of = h->local_of;
   return da;
 }
