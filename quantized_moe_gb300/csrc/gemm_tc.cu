@@ -410,11 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     for (int n = 0; n < RPW; ++n)
 #pragma unroll
       for (int j = 0; j < 4; ++j) aoff[n][j] = a_row_addr(0, wi + WPG * n, j);
-    uint32_t gs = 0;
+    uint32_t gs0 = 0;  // stages of the CTA's earlier items
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
-      for (int s = 0; s < n_stages; ++s, ++gs) {
-        if ((int)(gs % NG) != grp) continue;
+      // An item's stage count is a multiple of NG, so stage gs0 + s is this group's for s = grp,
+      // grp + NG, ...: the group steps over its own stages only.
+      for (int s = grp; s < n_stages; s += NG) {
+        const uint32_t gs = gs0 + s;
         // the raw units follow the stages: unit gs / kpu of the CTA's sequence (kpu == NG)
         const uint32_t gu = gs / kpu;
         const int rs = gu % RAWS, sa = gs % STAGES, su = gs % kpu;
@@ -444,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
       }
       if (!ok) break;
+      gs0 += n_stages;
     }
   } else {
     // ------------------------------------------------------------------ epilogue
