@@ -225,3 +225,43 @@ def test_batched_forward_with_every_token_table_routed():
     assert np.all(w == np.float32(1.0 / SMALL_MIX.top_k))
     assert int(st["counts"].sum()) == n * SMALL_MIX.top_k and st["error_flags"] == 0
     assert np.max(np.abs(got - ref["out"])) <= moe_gpu.tolerance(ref["out"])
+
+
+@pytest.mark.parametrize("n", [6, 40], ids=["decode", "batched"])
+def test_forward_captured_in_the_callers_graph(n):
+    """A forward is stream-ordered with no host synchronisation, so a caller can capture it in its
+    own CUDA graph: replays on new inputs (written into the captured buffer) equal direct forwards
+    bitwise, on the decode path and on the batched path."""
+    import torch
+
+    spec = SMALL_MIX.with_(n_tokens=n, n_hash=min(5, n))
+    p = synthetic.make_problem(spec)
+    h = moe_gpu.create(p, max_tokens=64)
+    try:
+        cap = torch.cuda.Stream()
+        x = torch.empty((n, spec.d), dtype=torch.int16, device="cuda")
+        tids = torch.from_numpy(np.ascontiguousarray(p.token_ids[:spec.n_hash])).cuda()
+        out = torch.empty((n, spec.d), dtype=torch.float32, device="cuda")
+
+        def run():
+            api.ds4moe_forward_ex(h, x.data_ptr(), n, tids.data_ptr(), spec.n_hash, out.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+
+        x.copy_(torch.from_numpy(synthetic.activations(spec.with_(seed=100)).view(np.int16)))
+        with torch.cuda.stream(cap):
+            run()  # warm-up outside the capture (first-use checks of the buffers)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            run()
+        for seed in (101, 102):
+            xb = synthetic.activations(spec.with_(seed=seed))
+            x.copy_(torch.from_numpy(xb.view(np.int16)))
+            out.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            got = out.cpu().numpy()
+            want, _, _ = moe_gpu.forward(h, p, x_bits=xb)
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), seed
+    finally:
+        api.ds4moe_destroy(h)
