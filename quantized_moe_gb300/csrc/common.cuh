@@ -14,26 +14,32 @@ namespace ds4 {
 //
 // Quantized matrices are repacked at create time into "units" of 16 rows (a row-group)
 // by one K-chunk, ordered tile-major: [row-tile of 128 rows][K-unit][row-group in tile][unit].
-// Inside a unit every warp lane finds the bits of its m16n8k16 A fragments contiguous, so a
-// warp streams a unit with coalesced 16-byte loads.
+// The layout serves two readers: a warp of the decode GEMV, where lane L = 4g + t loads the bits
+// of its m16n8k16 A fragments as one coalesced 16-byte piece ("region") per chunk, and a thread of
+// the prefill GEMM, which dequantizes one whole row and reads that row's half of a region (8
+// bytes) from shared memory. Region 4g + t of a chunk lies at position lane_region(g, t), which
+// permutes the four regions of each g so that the 8-byte row reads of a half-warp hit 32 distinct
+// banks; a warp's 16-byte loads still cover the chunk's 512 bytes exactly.
 //
 // Fragment map of mma.m16n8k16 (lane = 4*g + t): A register r holds row g + 8*(r&1) at
 // k = 2t + 8*(r>>1) (low half) and k+1 (high half); B register r holds k = 2t + 8*r (+1)
 // of column g; C element c holds row g + 8*(c>>1), column 2t + (c&1).
 //
 // Q2_K unit = 16 rows x 256 k (one super-block per row), 1344 bytes:
-//   [0, 1024)    quants of k-chunk 0 then k-chunk 1 (128 k each). In a chunk lane L owns
-//                bytes [16L, 16L+16) = 4 words; word r holds, for MMA i = 0..7 (sub-block
-//                8c+i), the 2-bit q of A register r at bits [2i, 2i+2) (low half, k) and
-//                [16+2i, 18+2i) (high half, k+1).
+//   [0, 1024)    quants of k-chunk 0 then k-chunk 1 (128 k each). Region (g, t) of a chunk holds
+//                4 words (row g, k-pair t), (row g, k-pair t+4), (row g+8, k-pair t),
+//                (row g+8, k-pair t+4): A registers 0, 2, 1, 3. A word holds, for sub-block
+//                i = 0..7 of the chunk, the 2-bit q at k = 16i + 2 * (k-pair) in bits [2i, 2i+2)
+//                (low half) and of k+1 in bits [16+2i, 18+2i) (high half).
 //   [1024, 1280) scale bytes of chunk 0 then chunk 1, lane L owns bytes [4L, 4L+4):
 //                (row g, sub 2t), (row g, sub 2t+1), (row g+8, sub 2t), (row g+8, sub 2t+1),
 //                sub counted inside the chunk; each byte keeps s in the low nibble, m high.
 //   [1280, 1344) row r (0..15): fp16 d, fp16 dmin.
 // Q8_0 unit = 16 rows x 128 k (four blocks per row), 2176 bytes:
-//   [0, 2048)    u = q + 128 as bytes. Load j = 0..3 covers MMAs 2j, 2j+1: lane L owns
-//                bytes [512j + 16L, +16): word 2m+h holds A registers 2h, 2h+1 of MMA 2j+m
-//                as (reg 2h low, reg 2h high, reg 2h+1 low, reg 2h+1 high) bytes.
+//   [0, 2048)    u = q + 128 as bytes, one 512-byte piece per 32-k block j (sub-blocks 2j,
+//                2j+1). Region (g, t) of block j holds 4 words: (row g, sub 2j), (row g,
+//                sub 2j+1), (row g+8, sub 2j), (row g+8, sub 2j+1), each with the bytes of
+//                k = 2t, 2t+1, 2t+8, 2t+9 of its sub-block.
 //   [2048, 2176) lane L owns bytes [4L, 4L+4): fp16 scale of (row g, block t), (row g+8, block t).
 constexpr int kRowGroup = 16;
 constexpr int kTileRows = 128;
@@ -51,6 +57,9 @@ __host__ __device__ constexpr int unit_k(int fmt) { return fmt == FMT_Q2_K ? kQ2
 __host__ __device__ constexpr int unit_bytes(int fmt) { return fmt == FMT_Q2_K ? kQ2kUnitBytes : kQ80UnitBytes; }
 __host__ __device__ constexpr int canon_block(int fmt) { return fmt == FMT_Q2_K ? 256 : 32; }
 __host__ __device__ constexpr int canon_block_bytes(int fmt) { return fmt == FMT_Q2_K ? 84 : 34; }
+
+// Position (in 16-byte regions) of region (g, t) inside a 512-byte chunk of quants.
+__host__ __device__ constexpr int lane_region(int g, int t) { return 4 * g + (t ^ ((g >> 1) & 3)); }
 
 // Byte offset of unit (row-group rg, K-unit kb) in a repacked matrix with n_kb K-units.
 __host__ __device__ inline size_t unit_offset(int rg, int kb, int n_kb, int ubytes) {
@@ -205,7 +214,7 @@ cudaError_t gemm_prepare();
 // TMA maps of one row-major fp16 activation buffer: 64 columns x 64 rows and x 128 rows per box
 // (a tile's rows are fetched with as few boxes as the two sizes allow).
 struct ActMaps {
-  CUtensorMap r64, r128;
+  CUtensorMap r16, r32, r64, r128;  // boxes of 64 columns x 16 / 32 / 64 / 128 rows
 };
 cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int m_tiles, int n_tiles,
                         cudaStream_t s);

@@ -683,16 +683,18 @@ struct RawUnit {
 template <int FMT>
 __device__ __forceinline__ void raw_load(RawUnit& b, const uint8_t* __restrict__ ub) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
+  const int off = 16 * lane_region(g, lane & 3);
   if (FMT == FMT_Q2_K) {
-    b.v[0] = ldg_nc_v4(ub + 16 * lane);
-    b.v[1] = ldg_nc_v4(ub + 512 + 16 * lane);
+    const uint4 q0 = ldg_nc_v4(ub + off), q1 = ldg_nc_v4(ub + 512 + off);
+    b.v[0] = make_uint4(q0.x, q0.z, q0.y, q0.w);  // the region's words in A register order
+    b.v[1] = make_uint4(q1.x, q1.z, q1.y, q1.w);
     b.w[0] = ldg_nc_u32(ub + kQ2kScOff + 4 * lane);
     b.w[1] = ldg_nc_u32(ub + kQ2kScOff + 128 + 4 * lane);
     b.w[2] = ldg_nc_u32(ub + kQ2kDdOff + 4 * g);
     b.w[3] = ldg_nc_u32(ub + kQ2kDdOff + 4 * (g + 8));
   } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b.v[j] = ldg_nc_v4(ub + 512 * j + 16 * lane);
+    for (int j = 0; j < 4; ++j) b.v[j] = ldg_nc_v4(ub + 512 * j + off);
     b.w[0] = ldg_nc_u32(ub + kQ80ScOff + 4 * lane);
   }
 }

@@ -5,23 +5,28 @@
 //   gate/up: the 128 rows interleave 64 gate rows and the 64 up rows of the same features, so
 //            the epilogue forms h = silu(g) * u for 64 features and writes it as fp16;
 //   down:    128 rows of d, written as fp32 per bucketed slot for the fixed-order combine.
-// The weight, activation and dequantized-tile pipelines run on across items, and the fp32
-// accumulator is double-buffered in TMEM (2 x 256 columns), so the epilogue of one item overlaps
-// the main loop of the next. Each K stage (64 wide) has one full barrier, completed by the
-// dequant group that wrote its A tile and by the activation TMA, and one empty barrier, completed
-// by the MMA commit; four stages are in flight.
+// The dequantized weight tile (the MMA's A operand) never touches shared memory: the dequant
+// warps write it into tensor memory (tcgen05.st) and the MMA reads A from there and only the
+// activation tile (B) from shared memory. Tensor memory holds two fp32 accumulators of 192
+// columns (the epilogue of one item overlaps the main loop of the next) and four A stages of 64 k
+// (32 columns each); shared memory holds four activation stages and the packed weight units.
+// Each K stage (64 wide) has one full barrier, completed by the dequant group that wrote its A
+// stage and by the activation TMA, and one empty barrier, completed by the MMA commit: the MMA
+// thread makes one wait and one commit per stage (its loop of barrier operations, not the tensor
+// pipe, bounds the stage rate).
 // Warp roles (23 warps):
 //   warp 0     weight producer: bulk-copies the packed weight units of each K unit (256 k for
 //              Q2_K, 128 k for Q8_0) of the tile's rows;
 //   warp 1     allocates TMEM; the converged warp runs the MMA loop and one elected lane issues
 //              the tcgen05.mma and commits of every stage;
 //   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
-//              K stage, in 128-row boxes and at most one 64-row box;
-//   warps 3-18 dequantize, in one group per K stage of a raw unit (four groups of four warps for
-//              Q2_K, two of eight for Q8_0) taking the stages round-robin: each warp turns its
-//              16-row groups' 64-wide K stage into fp16 weights in registers (exact small-integer
-//              quants, one fp16 FMA with the sub-block scale and min) and writes them with
-//              stmatrix straight into the swizzled A tile;
+//              K stage, exactly the MMA's N rows, in boxes of 128, 64, 32 and 16 rows;
+//   warps 3-18 dequantize, in four groups of four warps taking the K stages round-robin (group g
+//              owns A stage g). A warp may only access its TMEM lane quadrant (warp % 4), so the
+//              four warps of a group cover the tile's 128 rows, one row per thread: the thread
+//              reads its row's quants and scales of the stage from shared memory, forms the 64
+//              fp16 weights (exact small-integer quants, one fp16 FMA with the sub-block scale
+//              and min) and stores them as 32 columns of its TMEM lane;
 //   warps 19-22 epilogue: read the accumulator from TMEM (tcgen05.ld), one warp per lane
 //              quadrant, and release its buffer to the MMA.
 // Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
@@ -38,40 +43,41 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int BOX_ROWS = 64;                    // rows per activation TMA box (8 KB)
 constexpr int kDeqWarps = 16;
-constexpr int kFirstDeq = 3;  // warps 0-2: weight producer, MMA, activation producer
-constexpr int kEpiWarps = 4;  // warps 19-22: epilogue, one per TMEM lane quadrant
+constexpr int kDeqGroups = 4;  // groups of four warps (one per TMEM lane quadrant)
+constexpr int kFirstDeq = 3;   // warps 0-2: weight producer, MMA, activation producer
+constexpr int kEpiWarps = 4;   // warps 19-22: epilogue, one per TMEM lane quadrant
 constexpr int kThreads = (kFirstDeq + kDeqWarps + kEpiWarps) * 32;  // 736
-constexpr int ACC_COLS = 256;            // TMEM columns per accumulator (128 x N fp32, N <= 256)
-constexpr int TMEM_COLS = 2 * ACC_COLS;  // double-buffered: the epilogue of one item overlaps the next
 
-// Packed weight stages: eight 16-row units (one K unit of the 128-row tile) each; four stages of
-// Q2_K (256 k each) or three of Q8_0 (128 k each) keep the next units' HBM reads in flight.
-// Four K stages of 64 (A and B tiles) with token tiles of 192.
-#ifndef GEMM_STAGES
-#define GEMM_STAGES 4
-#endif
 #ifndef GEMM_BN
 #define GEMM_BN 192
 #endif
+// Tensor memory: two accumulators of BN fp32 columns, then the A stages (64 k of fp16 = 32 columns)
+// in the columns left over.
+constexpr int ACC_COLS = GEMM_BN;
+constexpr int A_COLS = BK / 2;
+constexpr int A_COL0 = 2 * ACC_COLS;
+constexpr int TMEM_COLS = 512;
+#ifndef GEMM_ASTAGES
+#define GEMM_ASTAGES ((TMEM_COLS - 2 * GEMM_BN) / (BK / 2) < 8 ? (TMEM_COLS - 2 * GEMM_BN) / (BK / 2) : 8)
+#endif
+constexpr int A_STAGES = GEMM_ASTAGES;
+static_assert(A_COL0 + A_STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
+
 template <int FMT>
 struct Cfg {
-  static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);
-  static constexpr int RAWS = FMT == FMT_Q2_K ? 4 : 3;
-  // Token tile (MMA N at most): 192 tokens, so that four K stages fit in shared memory beside the
-  // raw weight stages.
+  static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);  // one K unit of the 128-row tile
+  static constexpr int RAWS = 4;                         // K units in flight
+  // Token tile (MMA N at most): 192 tokens.
   static constexpr int BN = GEMM_BN;
   static constexpr int B_BYTES = BN * BK * 2;
-  // K stages in flight: each holds a dequantized weight tile (A) and an activation tile (B)
-  static constexpr int STAGES = GEMM_STAGES;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
-  static_assert(BN % BOX_ROWS == 0 && BN <= ACC_COLS, "token tile");
+  // activation stages in shared memory, one per A stage in tensor memory
+  static constexpr int B_STAGES = A_STAGES;
+  static constexpr int OFF_B = 0;
+  static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
+  static_assert(BN <= 256 && BN % 16 == 0, "token tile");
   static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
-  static constexpr int N_BARS = 2 * STAGES + 2 * RAWS + 4;
+  static constexpr int N_BARS = 2 * A_STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
   // gate/up epilogue: two parities x (8 columns of g + 8 columns of u) x 64 features fp32, then the
@@ -81,11 +87,9 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// One full/empty pair per K stage for both operands: the MMA thread makes one wait and one commit
-// per stage, and the dequant warps and the activation producer wait on the same release.
 struct Bars {
-  uint64_t* full;       // [STAGES] dequant group (A) + activation TMA (B, with its bytes) -> MMA
-  uint64_t* empty;      // [STAGES] MMA commit -> dequant group and activation producer
+  uint64_t* full;       // [A_STAGES] the dequant group's four warps + activation TMA (with its bytes) -> MMA
+  uint64_t* empty;      // [A_STAGES] MMA commit -> dequant group and activation producer
   uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
   uint64_t* raw_empty;  // [RAWS] dequant -> producer
   uint64_t* acc_full;   // [2] MMA -> epilogue
@@ -99,86 +103,77 @@ __device__ __forceinline__ float silu_mul_fast(float g, float u) { return __fdiv
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// stmatrix row address of this lane for the 16x16 block (row group rg16 of the tile, 16-k
-// sub-block sb of the 64-k stage) in the 128-byte swizzled A tile.
-__device__ __forceinline__ uint32_t a_row_addr(uint32_t a_base, int rg16, int sb) {
-  const int lane = threadIdx.x & 31, j = lane >> 3, q = lane & 7;
-  const int row = 16 * rg16 + q + 8 * (j & 1);
-  const int kc = 2 * sb + (j >> 1);  // 16-byte chunk of the 128-byte row
-  return a_base + (row >> 3) * 1024 + (row & 7) * 128 + ((kc ^ (row & 7)) << 4);
-}
-
-// Per-row constants of a Q2_K unit for this lane's rows (g, g+8): 2^16 d (exact: only the exponent
-// changes; create refuses super-blocks whose 2^16 d * 15 would leave the fp16 range), -dmin and
-// 1024 dmin (m is read as the fp16 1024 + m, so one FMA gives -dmin * m rounded once).
-struct Q2kRowConst {
-  __half2 d2, ndm2, dm1024;
-};
-
-__device__ __forceinline__ Q2kRowConst q2k_row_const(uint32_t unit) {
-  const int g = (threadIdx.x & 31) >> 2;
-  const uint32_t dd0 = lds32(unit + kQ2kDdOff + 4 * g), dd1 = lds32(unit + kQ2kDdOff + 4 * (g + 8));
-  const __half2 k256 = __float2half2_rn(256.f);
-  const __half2 dm2 = u2h(prmt(dd0, dd1, 0x7632u));  // (dmin of row g, dmin of row g+8)
-  Q2kRowConst r;
-  r.d2 = __hmul2(__hmul2(u2h(prmt(dd0, dd1, 0x5410u)), k256), k256);
-  r.ndm2 = __hneg2(dm2);
-  r.dm1024 = __hmul2(dm2, __float2half2_rn(1024.f));
-  return r;
-}
-
-// All four 16-k sub-blocks I0..I0+3 of a Q2_K stage for this lane's rows in each of the warp's NR
-// 16-row groups: the arithmetic of every (group, sub-block) pair is independent and interleaves,
-// then the stores follow.
-template <int I0, int NR>
-__device__ __forceinline__ void deq_q2k_quad(const uint32_t (&w)[NR][4], const uint32_t (&sc01)[NR],
-                                             const uint32_t (&sc23)[NR], const Q2kRowConst (&rc)[NR],
-                                             uint32_t a_base, const uint32_t (&aoff)[NR][4]) {
-  const __half2 k1024 = __float2half2_rn(1024.f);
-  uint32_t a[NR][4][4];
+// One row of one K stage of a Q2_K unit: 64 fp16 weights as 32 columns, column 8i + kp holding
+// k = 16i + 2kp and k + 1 of the stage (sub-block i = 0..3, k-pair kp = 0..7). The stage is half
+// H of chunk c; its sub-blocks are fields 4H .. 4H + 3 of the row's eight k-pair words.
+// Each field is shifted to bits 8-9 of its half: as an fp16 subnormal that is q * 2^-16, and the
+// sub-block scale carries 2^16 d * s (exact: only the exponent changes; create refuses
+// super-blocks whose 2^16 d * 15 would leave the fp16 range), so one FMA with the min gives
+// d s q - dmin m rounded once.
+template <int H>
+__device__ __forceinline__ void deq_q2k_row(uint32_t unit, int c, int g, int ah, uint32_t (&v)[32]) {
+  const int sw = (g >> 1) & 3;
+  uint32_t w[8];  // k-pair kp of this row: the chunk's eight sub-blocks, 2 bits each per half
 #pragma unroll
-  for (int n = 0; n < NR; ++n) {
+  for (int t = 0; t < 4; ++t) {
+    const uint2 x = lds64(unit + c * 512 + 16 * (4 * g + (t ^ sw)) + 8 * ah);
+    w[t] = x.x;
+    w[t + 4] = x.y;
+  }
+  // scale words 2H and 2H + 1 of the chunk hold sub-blocks 4H .. 4H + 3 in bytes 2ah, 2ah + 1
+  const uint4 scw = lds128(unit + kQ2kScOff + c * 128 + 16 * g);
+  const uint32_t dd = lds32(unit + kQ2kDdOff + 4 * (g + 8 * ah));  // fp16 d, dmin of the row
+  const __half2 k256 = __float2half2_rn(256.f), k1024 = __float2half2_rn(1024.f);
+  const __half2 d16 = __hmul2(__hmul2(__low2half2(u2h(dd)), k256), k256);
+  const __half2 dm = __high2half2(u2h(dd));
+  const __half2 ndm = __hneg2(dm), dm1024 = __hmul2(dm, k1024);
+  const uint32_t sel = ah ? 0x4342u : 0x4140u;
+  __half2 ds[4], nm[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int sh = 8 - 2 * (I0 + j);  // left shift of sub-block I0 + j's field (negative: right)
-      const uint32_t sc = (j < 2 ? sc01[n] : sc23[n]) >> (8 * (j & 1));
-      const __half2 ds = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), rc[n].d2);
-      const __half2 ndm = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), rc[n].ndm2, rc[n].dm1024);
+  for (int p = 0; p < 2; ++p) {
+    const uint32_t sc = prmt(p == 0 ? (H ? scw.z : scw.x) : (H ? scw.w : scw.y), 0u, sel);  // (sub 2p, sub 2p+1)
+    const __half2 s2 = __hmul2(__hsub2(u2h((sc & 0x000F000Fu) | 0x64006400u), k1024), d16);
+    const __half2 m2 = __hfma2(u2h(((sc >> 4) & 0x000F000Fu) | 0x64006400u), ndm, dm1024);
+    ds[2 * p] = __low2half2(s2);
+    ds[2 * p + 1] = __high2half2(s2);
+    nm[2 * p] = __low2half2(m2);
+    nm[2 * p + 1] = __high2half2(m2);
+  }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t qb = (sh >= 0 ? (w[n][r] << sh) : (w[n][r] >> -sh)) & 0x03000300u;
-        a[n][j][r] = h2u((r & 1) ? __hfma2(u2h(qb), __high2half2(ds), __high2half2(ndm))
-                                 : __hfma2(u2h(qb), __low2half2(ds), __low2half2(ndm)));
-      }
+  for (int i = 0; i < 4; ++i) {
+    const int f = 4 * H + i;        // field of sub-block i in the k-pair words
+    const int sh = 8 - 2 * f;       // left shift to bits 8-9 (negative: right)
+#pragma unroll
+    for (int kp = 0; kp < 8; ++kp) {
+      const uint32_t qb = (sh >= 0 ? (w[kp] << sh) : (w[kp] >> -sh)) & 0x03000300u;
+      v[8 * i + kp] = h2u(__hfma2(u2h(qb), ds[i], nm[i]));
     }
   }
-#pragma unroll
-  for (int n = 0; n < NR; ++n)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) stmatrix_x4(a_base + aoff[n][j], a[n][j][0], a[n][j][1], a[n][j][2], a[n][j][3]);
 }
 
-// The 16 rows x 64 k of K stage su (0..3) of NR Q2_K units (one per 16-row group of the warp).
-template <int NR>
-__device__ __forceinline__ void deq_q2k_stage(const uint32_t (&unit)[NR], int su, uint32_t a_base,
-                                              const uint32_t (&aoff)[NR][4], const Q2kRowConst (&rc)[NR]) {
-  const int lane = threadIdx.x & 31, g = lane >> 2;
-  const int c = su >> 1, i0 = (su & 1) * 4;
-  uint32_t w[NR][4], sc01[NR], sc23[NR];
+// One row of one K stage (half H of the unit: 32-k blocks 2H, 2H + 1) of a Q8_0 unit, in the
+// column order of deq_q2k_row: fp16 (1024 + u) by byte permutation, minus 1152 gives q exactly,
+// times the block scale.
+template <int H>
+__device__ __forceinline__ void deq_q80_row(uint32_t unit, int g, int ah, uint32_t (&v)[32]) {
+  const int sw = (g >> 1) & 3;
+  const uint2 scw = lds64(unit + kQ80ScOff + 16 * g + 8 * H);  // blocks 2H, 2H+1: (row g, row g+8)
+  const __half2 k1152 = __float2half2_rn(1152.f);
 #pragma unroll
-  for (int n = 0; n < NR; ++n) {
-    const uint4 qw = lds128(unit[n] + c * 512 + 16 * lane);
-    w[n][0] = qw.x;
-    w[n][1] = qw.y;
-    w[n][2] = qw.z;
-    w[n][3] = qw.w;
-    sc01[n] = lds32(unit[n] + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2));
-    sc23[n] = lds32(unit[n] + kQ2kScOff + c * 128 + 4 * (4 * g + i0 / 2 + 1));
+  for (int jl = 0; jl < 2; ++jl) {
+    const uint32_t sw32 = jl == 0 ? scw.x : scw.y;
+    const __half2 s = ah ? __high2half2(u2h(sw32)) : __low2half2(u2h(sw32));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint2 x = lds64(unit + 512 * (2 * H + jl) + 16 * (4 * g + (t ^ sw)) + 8 * ah);
+      // x.x: sub-block 2j, x.y: sub-block 2j + 1; bytes k = 2t, 2t+1, 2t+8, 2t+9
+      const uint32_t raw[4] = {prmt(x.x, 0x64u, 0x4140u), prmt(x.x, 0x64u, 0x4342u), prmt(x.y, 0x64u, 0x4140u),
+                               prmt(x.y, 0x64u, 0x4342u)};
+      const int col[4] = {16 * jl + t, 16 * jl + t + 4, 16 * jl + 8 + t, 16 * jl + 12 + t};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[col[e]] = h2u(__hmul2(__hsub2(u2h(raw[e]), k1152), s));
+    }
   }
-  if (i0 == 0)
-    deq_q2k_quad<0, NR>(w, sc01, sc23, rc, a_base, aoff);
-  else
-    deq_q2k_quad<4, NR>(w, sc01, sc23, rc, a_base, aoff);
 }
 
 // Waits (bounded, without raising errors) for a phase: used only to let copies land, or issued MMAs
@@ -189,19 +184,18 @@ __device__ __forceinline__ void bounded_try(uint64_t* bar, uint32_t parity, long
   }
 }
 
-// mbar_wait by lane 0 of a converged warp, its result given to every lane.
-__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site,
-                                           long long limit) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err, site, limit);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+// mbar_wait by every lane of a converged warp: no divergent branch and no shuffle to hand the
+// result over (a lane-0 wait plus shuffle cost the MMA loop about 100 cycles per stage).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site,
+                                          long long limit) {
+  return mbar_wait(bar, parity, abort_flag, err, site, limit);
 }
 
-// The tile of work item `it` (token tile, 128-row slice of the weights): `nbox` activation boxes
-// of 64 rows are loaded, and the MMA's N (the accumulator columns the epilogue reads) is the row
-// count rounded up to the instruction's granularity of 16, not to the box.
+// The tile of work item `it` (token tile, 128-row slice of the weights): the MMA's N (the
+// activation rows loaded and the accumulator columns the epilogue reads) is the row count rounded
+// up to the instruction's granularity of 16.
 struct Item {
-  int expert, row0, rows, nbox, n, mt;
+  int expert, row0, rows, n, mt;
 };
 
 template <int BN>
@@ -219,7 +213,6 @@ __device__ __forceinline__ Item item_of(const GemmArgs& p, int it) {
     t.row0 = tile * BN;
     t.rows = min(BN, p.n_rows - t.row0);
   }
-  t.nbox = (max(t.rows, 1) + BOX_ROWS - 1) / BOX_ROWS;
   t.n = (max(t.rows, 1) + 15) / 16 * 16;
   return t;
 }
@@ -232,48 +225,19 @@ __device__ __forceinline__ int item_count(const GemmArgs& p) {
   return tiles * p.m_tiles;
 }
 
-// The 16 rows x 64 k of one Q8_0 unit (128 k) that fall in K stage su (0..1): loads first, then
-// the four sub-blocks, then the stores.
-__device__ __forceinline__ void deq_q80_stage(uint32_t unit, int su, uint32_t a_base, const uint32_t (&aoff)[4]) {
-  const int lane = threadIdx.x & 31, g = lane >> 2;
-  const __half2 k1152 = __float2half2_rn(1152.f);
-  uint4 v[2];
-  uint32_t scw[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {  // 32-weight block 2 su + h: sub-blocks 2h, 2h + 1 of the stage
-    v[h] = lds128(unit + 512 * (2 * su + h) + 16 * lane);
-    scw[h] = lds32(unit + kQ80ScOff + 4 * (4 * g + 2 * su + h));
-  }
-  uint32_t a[4][4];
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const uint4 vv = v[ii >> 1];
-    const uint32_t wa = (ii & 1) ? vv.z : vv.x, wb = (ii & 1) ? vv.w : vv.y;
-    const __half2 sc = u2h(scw[ii >> 1]);  // (row g, row g+8)
-    const uint32_t raw[4] = {prmt(wa, 0x64u, 0x4140u), prmt(wa, 0x64u, 0x4342u), prmt(wb, 0x64u, 0x4140u),
-                             prmt(wb, 0x64u, 0x4342u)};  // fp16 1024 + u, u = q + 128
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      a[ii][r] = h2u(__hmul2(__hsub2(u2h(raw[r]), k1152), (r & 1) ? __high2half2(sc) : __low2half2(sc)));
-  }
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii) stmatrix_x4(a_base + aoff[ii], a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
-}
-
 template <int FMT, bool GATEUP>
-__global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap64,
+__global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap16,
+                                                                      const __grid_constant__ CUtensorMap tmap32,
+                                                                      const __grid_constant__ CUtensorMap tmap64,
                                                                       const __grid_constant__ CUtensorMap tmap128,
                                                                       GemmArgs p) {
   using C = Cfg<FMT>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS;
-  constexpr int STAGES = C::STAGES;
-  // dequant groups (one per K stage of a raw unit), warps per group, 16-row groups per warp
-  constexpr int NG = UK / BK, WPG = kDeqWarps / NG, RPW = 8 / WPG;
-  static_assert(NG <= STAGES && WPG * RPW == 8, "dequant groups");
-  const int n_kb = p.k / UK, n_stages = p.k / BK, kpu = UK / BK;
+  constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS, BS = C::B_STAGES;
+  constexpr int kpu = UK / BK;  // K stages per raw unit: Q2_K four, Q8_0 two
+  const int n_kb = p.k / UK, n_stages = p.k / BK;
   const int n_items = item_count<C::BN>(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
   const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
@@ -282,24 +246,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   Bars b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   b.full = bars;
-  b.empty = bars + STAGES;
-  b.raw_full = bars + 2 * STAGES;
+  b.empty = b.full + A_STAGES;
+  b.raw_full = b.empty + A_STAGES;
   b.raw_empty = b.raw_full + RAWS;
-  b.acc_full = b.raw_empty + RAWS;   // [2]
-  b.acc_empty = b.acc_full + 2;      // [2]
+  b.acc_full = b.raw_empty + RAWS;  // [2]
+  b.acc_empty = b.acc_full + 2;     // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* gbuf = reinterpret_cast<float*>(smem + C::OFF_GBUF);
   float* ibuf = gbuf + 2048;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&b.full[i], WPG + 1);  // one group of dequant warps + the activation producer
+    for (int i = 0; i < A_STAGES; ++i) {
+      mbar_init(&b.full[i], kDeqWarps / kDeqGroups + 1);  // the four warps of one dequant group + TMA
       mbar_init(&b.empty[i], 1);
     }
     for (int r = 0; r < RAWS; ++r) {
       mbar_init(&b.raw_full[r], 1);
-      mbar_init(&b.raw_empty[r], kDeqWarps);
+      mbar_init(&b.raw_empty[r], (kDeqWarps / kDeqGroups) * kpu);  // every warp of the unit's kpu stages
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.acc_full[i], 1);
@@ -347,46 +311,48 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
         const Item t = item_of<C::BN>(p, it);
         for (int sB = 0; sB < n_stages; ++sB, ++gs) {
-          const int sb = gs % STAGES;
-          if (!mbar_wait(&b.empty[sb], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
+          const int sb = gs % BS;
+          if (!mbar_wait(&b.empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
-          const int rows = t.nbox * BOX_ROWS;  // rows fetched: 128-row boxes, then a 64-row one
+          // exactly the MMA's N rows: 128-row boxes, then at most one box each of 64, 32 and 16
+          const int rows = t.n;
           mbar_expect_tx(&b.full[sb], rows * BK * 2);
           int r = 0;
-          for (; rows - r >= 2 * BOX_ROWS; r += 2 * BOX_ROWS)
-            tma_load_2d(bdst + r * BK * 2, &tmap128, sB * BK, t.row0 + r, &b.full[sb]);
-          if (r < rows) tma_load_2d(bdst + r * BK * 2, &tmap64, sB * BK, t.row0 + r, &b.full[sb]);
+          for (; rows - r >= 128; r += 128) tma_load_2d(bdst + r * BK * 2, &tmap128, sB * BK, t.row0 + r, &b.full[sb]);
+          if (rows - r >= 64) { tma_load_2d(bdst + r * BK * 2, &tmap64, sB * BK, t.row0 + r, &b.full[sb]); r += 64; }
+          if (rows - r >= 32) { tma_load_2d(bdst + r * BK * 2, &tmap32, sB * BK, t.row0 + r, &b.full[sb]); r += 32; }
+          if (rows - r >= 16) tma_load_2d(bdst + r * BK * 2, &tmap16, sB * BK, t.row0 + r, &b.full[sb]);
         }
       }
-      for (uint32_t k = gs > (uint32_t)STAGES ? gs - STAGES : 0; k < gs; ++k)
-        bounded_try(&b.full[k % STAGES], (k / STAGES) & 1, limit);
+      for (uint32_t k = gs > (uint32_t)BS ? gs - BS : 0; k < gs; ++k)
+        bounded_try(&b.full[k % BS], (k / BS) & 1, limit);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop; lane 0 polls the barriers and one elected lane issues.
+    // The whole warp runs the loop and polls the barriers; one elected lane issues.
     uint32_t gs = 0;
     int local = 0;  // items of this CTA so far: accumulator buffer local & 1
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++local) {
       const Item t = item_of<C::BN>(p, it);
       const int buf = local & 1;
       // the epilogue has drained this buffer (item local - 2)
-      if (!lane0_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6, limit)) break;
+      if (!warp_wait(&b.acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 6, limit)) break;
       tc_fence_after();
       const uint32_t idesc = idesc_f16_f32(BM, t.n);
       const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS);
       bool ok = true;
       for (int s = 0; s < n_stages; ++s, ++gs) {
-        const int st = gs % STAGES;
-        if (!lane0_wait(&b.full[st], (gs / STAGES) & 1, abort_flag, p.err, 7, limit)) {
+        const int st = gs % A_STAGES;
+        if (!warp_wait(&b.full[st], (gs / A_STAGES) & 1, abort_flag, p.err, 7, limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_desc(su32(smem + C::OFF_A + st * A_BYTES));
+        const uint32_t ta = tmem + (uint32_t)(A_COL0 + st * A_COLS);
         const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + st * C::B_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 fp16 = 32 bytes along K per MMA
-          tc_mma_f16_elect(acc, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+        for (int kk = 0; kk < BK / 16; ++kk)  // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
+          tc_mma_f16_ts_elect(acc, ta + 8 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
         tc_commit_elect(&b.empty[st]);
       }
       if (!ok) break;
@@ -394,55 +360,52 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     }
     // After an abort, the MMAs already issued must finish before TMEM is freed: the commit of the
     // last issued stage (stage gs - 1) arrives only once all of them have completed.
-    if (*abort_flag && gs > 0 && lane == 0) bounded_try(&b.empty[(gs - 1) % STAGES], ((gs - 1) / STAGES) & 1, limit);
+    if (*abort_flag && gs > 0 && lane == 0) bounded_try(&b.empty[(gs - 1) % BS], ((gs - 1) / BS) & 1, limit);
     __syncwarp();
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
-    // NG groups of warps take K stages round-robin, NG = the stages per raw unit (Q2_K four, Q8_0
-    // two), so each group dequantizes one stage of every unit and NG stages are in progress at
-    // once. In a stage, each warp of a group turns all four 16-k sub-blocks of its RPW 16-row
-    // groups into fp16: 4 * RPW independent pieces of work per lane.
+    // Four groups of four warps take the CTA's K stages round-robin: group g dequantizes the
+    // stages gs = g (mod 4), each into A stage gs (mod A_STAGES). Warp w accesses TMEM lanes
+    // 32 (w % 4) .. + 31, and a group's four consecutive warps cover all four quadrants; a thread
+    // owns tile row = its lane.
     const int dw = warp - kFirstDeq;
-    const int grp = dw / WPG, wi = dw % WPG;
-    // this lane's stmatrix row offsets for the sub-blocks of a stage (fixed per warp)
-    uint32_t aoff[RPW][4];
-#pragma unroll
-    for (int n = 0; n < RPW; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) aoff[n][j] = a_row_addr(0, wi + WPG * n, j);
+    const int grp = dw / (kDeqWarps / kDeqGroups);
+    const int quad = warp & 3;
+    const int row = 32 * quad + lane;                      // tile row = TMEM lane
+    const int rho = row & 15, g = rho & 7, ah = rho >> 3;  // row inside its 16-row unit
+    const uint32_t t_q = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)A_COL0;
     uint32_t gs0 = 0;  // stages of the CTA's earlier items
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
-      // An item's stage count is a multiple of NG, so stage gs0 + s is this group's for s = grp,
-      // grp + NG, ...: the group steps over its own stages only.
-      for (int s = grp; s < n_stages; s += NG) {
+      for (int s = (grp - (int)(gs0 % kDeqGroups) + kDeqGroups) % kDeqGroups; s < n_stages; s += kDeqGroups) {
         const uint32_t gs = gs0 + s;
-        // the raw units follow the stages: unit gs / kpu of the CTA's sequence (kpu == NG)
-        const uint32_t gu = gs / kpu;
-        const int rs = gu % RAWS, sa = gs % STAGES, su = gs % kpu;
+        const uint32_t gu = gs / kpu;  // the raw units follow the stages
+        const int rs = gu % RAWS, su = gs % kpu;
         if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3, limit)) { ok = false; break; }
-        if (!mbar_wait(&b.empty[sa], ((gs / STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
-        const uint32_t raw = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES);
-        const uint32_t a_base = su32(smem + C::OFF_A + sa * A_BYTES);
+        const int sa = gs % A_STAGES;
+        if (!mbar_wait(&b.empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES) + (row >> 4) * UB;
+        uint32_t v[32];
         if constexpr (FMT == FMT_Q2_K) {
-          uint32_t unit[RPW];
-          Q2kRowConst rc[RPW];
-#pragma unroll
-          for (int n = 0; n < RPW; ++n) {
-            unit[n] = raw + (wi + WPG * n) * UB;
-            rc[n] = q2k_row_const(unit[n]);
-          }
-          deq_q2k_stage<RPW>(unit, su, a_base, aoff, rc);
+          if (su & 1)
+            deq_q2k_row<1>(unit, su >> 1, g, ah, v);
+          else
+            deq_q2k_row<0>(unit, su >> 1, g, ah, v);
         } else {
-#pragma unroll
-          for (int n = 0; n < RPW; ++n) deq_q80_stage(raw + (wi + WPG * n) * UB, su, a_base, aoff[n]);
+          if (su & 1)
+            deq_q80_row<1>(unit, g, ah, v);
+          else
+            deq_q80_row<0>(unit, g, ah, v);
         }
-        fence_proxy_async();  // the generic-proxy stores must be visible to the tensor core
+        tmem_st32(t_q + (uint32_t)(sa * A_COLS), v);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           // (a test of the timeout path withholds one arrival: that stage never becomes full)
           if (!(p.test_stall && blockIdx.x == 0 && gs + 1 == (uint32_t)p.test_stall)) mbar_arrive(&b.full[sa]);
-          mbar_arrive(&b.raw_empty[rs]);  // the group's only stage of this unit is done
+          mbar_arrive(&b.raw_empty[rs]);
         }
       }
       if (!ok) break;
@@ -519,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
 template <int FMT, bool GATEUP>
 cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
-  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm.r64, tm.r128, p);
+  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm.r16, tm.r32, tm.r64, tm.r128, p);
   return cudaGetLastError();
 }
 
@@ -580,8 +543,10 @@ int make_tmap_f16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t col
 }
 
 int make_act_maps(ActMaps* tm, const void* base, uint64_t rows, uint64_t cols) {
-  const int r = make_tmap_f16(&tm->r64, base, rows, cols, BOX_ROWS);
-  return r ? r : make_tmap_f16(&tm->r128, base, rows, cols, 2 * BOX_ROWS);
+  int r = make_tmap_f16(&tm->r16, base, rows, cols, 16);
+  if (!r) r = make_tmap_f16(&tm->r32, base, rows, cols, 32);
+  if (!r) r = make_tmap_f16(&tm->r64, base, rows, cols, 64);
+  return r ? r : make_tmap_f16(&tm->r128, base, rows, cols, 128);
 }
 
 }  // namespace ds4

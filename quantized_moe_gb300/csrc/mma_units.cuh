@@ -189,10 +189,10 @@ __device__ __forceinline__ void q80_chunk_mma(const uint4 (&v)[4], const BMask& 
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int j = i >> 1;
-    const uint32_t wa = (i & 1) ? v[j].z : v[j].x;  // registers 0, 1
-    const uint32_t wb = (i & 1) ? v[j].w : v[j].y;  // registers 2, 3
-    const uint32_t a[4] = {prmt(wa, 0u, 0x4140u), prmt(wa, 0u, 0x4342u), prmt(wb, 0u, 0x4140u),
-                           prmt(wb, 0u, 0x4342u)};
+    const uint32_t wg = (i & 1) ? v[j].y : v[j].x;   // row g of sub-block i: k 2t, 2t+1, 2t+8, 2t+9
+    const uint32_t wg8 = (i & 1) ? v[j].w : v[j].z;  // row g + 8
+    const uint32_t a[4] = {prmt(wg, 0u, 0x4140u), prmt(wg8, 0u, 0x4140u), prmt(wg, 0u, 0x4342u),
+                           prmt(wg8, 0u, 0x4342u)};
     if (i & 1)
       mma_f16_16816(e, a, bsel(x.b0, bm.m[i]), bsel(x.b1, bm.m[i]));
     else
@@ -210,9 +210,11 @@ struct Q2kUnitRegs {
 
 __device__ __forceinline__ Q2kUnitRegs q2k_load(const uint8_t* __restrict__ ub) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
+  const int off = 16 * lane_region(g, lane & 3);
+  const uint4 q0 = ldg_nc_v4(ub + off), q1 = ldg_nc_v4(ub + 512 + off);
   Q2kUnitRegs r;
-  r.q[0] = ldg_nc_v4(ub + 16 * lane);
-  r.q[1] = ldg_nc_v4(ub + 512 + 16 * lane);
+  r.q[0] = make_uint4(q0.x, q0.z, q0.y, q0.w);  // the region's words in A register order
+  r.q[1] = make_uint4(q1.x, q1.z, q1.y, q1.w);
   r.sc[0] = ldg_nc_u32(ub + kQ2kScOff + 4 * lane);
   r.sc[1] = ldg_nc_u32(ub + kQ2kScOff + 128 + 4 * lane);
   r.dd0 = ldg_nc_u32(ub + kQ2kDdOff + 4 * g);
@@ -227,9 +229,10 @@ struct Q80UnitRegs {
 
 __device__ __forceinline__ Q80UnitRegs q80_load(const uint8_t* __restrict__ ub) {
   const int lane = threadIdx.x & 31;
+  const int off = 16 * lane_region(lane >> 2, lane & 3);
   Q80UnitRegs r;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) r.v[j] = ldg_nc_v4(ub + 512 * j + 16 * lane);
+  for (int j = 0; j < 4; ++j) r.v[j] = ldg_nc_v4(ub + 512 * j + off);
   r.sc = ldg_nc_u32(ub + kQ80ScOff + 4 * lane);
   return r;
 }

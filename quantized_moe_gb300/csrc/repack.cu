@@ -1,5 +1,5 @@
-// Create-time repack of canonical Q2_K / Q8_0 rows into the fragment-ordered units that the
-// GEMV kernels stream (layout described in common.cuh). One thread writes one 32-bit word.
+// Create-time repack of canonical Q2_K / Q8_0 rows into the units that the decode GEMV and the
+// prefill GEMM read (layout described in common.cuh). One thread writes one 32-bit word.
 #include "common.cuh"
 
 namespace ds4 {
@@ -22,11 +22,11 @@ __global__ void repack_q2k_kernel(const uint8_t* __restrict__ src, uint8_t* __re
     const int rg = (int)(u / n_kb), kb = (int)(u % n_kb);
     const uint8_t* rowblk = src + (size_t)(rg * 16) * row_bytes + (size_t)kb * 84;  // row 0 of the group
     uint32_t word = 0;
-    if (w < 256) {  // quants
-      const int c = w / 128, lane = (w % 128) / 4, r = w % 4;
-      const int g = lane >> 2, t = lane & 3;
-      const int row = g + 8 * (r & 1);
-      const int koff = 2 * t + 8 * (r >> 1);
+    if (w < 256) {  // quants: region (g, t) at position lane_region(g, t), words (row half, k-pair half)
+      const int c = w / 128, pos = (w % 128) / 4, r = w % 4;
+      const int g = pos >> 2, t = (pos & 3) ^ ((g >> 1) & 3);
+      const int row = g + 8 * (r >> 1);
+      const int koff = 2 * t + 8 * (r & 1);
       const uint8_t* blk = rowblk + (size_t)row * row_bytes;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -64,15 +64,13 @@ __global__ void repack_q80_kernel(const uint8_t* __restrict__ src, uint8_t* __re
     const int rg = (int)(u / n_kb), kb = (int)(u % n_kb);
     const uint8_t* row0 = src + (size_t)(rg * 16) * row_bytes;
     uint32_t word = 0;
-    if (w < 512) {
-      const int j = w / 128, lane = (w % 128) / 4, ww = w % 4;
-      const int g = lane >> 2, t = lane & 3;
-      const int i = 2 * j + (ww >> 1), h = ww & 1;
+    if (w < 512) {  // region (g, t) at position lane_region(g, t): words (row half, sub-block)
+      const int j = w / 128, pos = (w % 128) / 4, ww = w % 4;
+      const int g = pos >> 2, t = (pos & 3) ^ ((g >> 1) & 3);
+      const int row = g + 8 * (ww >> 1), i = 2 * j + (ww & 1);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {  // bytes: reg 2h lo, reg 2h hi, reg 2h+1 lo, reg 2h+1 hi
-        const int reg = 2 * h + (e >> 1);
-        const int row = g + 8 * (reg & 1);
-        const int kk = kb * 128 + 16 * i + 2 * t + 8 * (reg >> 1) + (e & 1);
+      for (int e = 0; e < 4; ++e) {  // bytes: k = 2t, 2t + 1, 2t + 8, 2t + 9 of sub-block i
+        const int kk = kb * 128 + 16 * i + 2 * t + 8 * (e >> 1) + (e & 1);
         const uint8_t qb = row0[(size_t)row * row_bytes + (size_t)(kk / 32) * 34 + 2 + (kk % 32)];
         word |= (uint32_t)(uint8_t)(qb ^ 0x80u) << (8 * e);  // u = q + 128
       }
