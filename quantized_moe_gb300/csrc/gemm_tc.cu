@@ -8,25 +8,28 @@
 // The dequantized weight tile (the MMA's A operand) never touches shared memory: the dequant
 // warps write it into tensor memory (tcgen05.st) and the MMA reads A from there and only the
 // activation tile (B) from shared memory. Tensor memory holds two fp32 accumulators of 192
-// columns (the epilogue of one item overlaps the main loop of the next) and four A stages of 64 k
-// (32 columns each); shared memory holds four activation stages and the packed weight units.
-// Each K stage (64 wide) has one full barrier, completed by the dequant group that wrote its A
-// stage and by the activation TMA, and one empty barrier, completed by the MMA commit: the MMA
-// thread makes one wait and one commit per stage (its loop of barrier operations, not the tensor
-// pipe, bounds the stage rate).
+// columns (the epilogue of one item overlaps the main loop of the next) and two pipeline stages of
+// A (128 k = 64 columns each); shared memory holds two activation stages and the packed weight
+// units. A pipeline stage is two 64-k sub-tiles (one 128-byte swizzle span each). It has one full
+// barrier, completed by the two dequant groups that wrote its A sub-tiles and by the activation
+// TMA, and one empty barrier, completed by the MMA commit: the MMA thread makes one wait and one
+// commit per eight MMAs (the loop of barrier operations, more than the tensor pipe, bounds the
+// stage rate, so a stage carries as much MMA work as tensor memory allows).
+// With an even number of weight slices the CTAs run in clusters of two on adjacent slices of the
+// same token tile and each loads half of every activation stage, multicast to both.
 // Warp roles (23 warps):
 //   warp 0     weight producer: bulk-copies the packed weight units of each K unit (256 k for
 //              Q2_K, 128 k for Q8_0) of the tile's rows;
 //   warp 1     allocates TMEM; the converged warp runs the MMA loop and one elected lane issues
 //              the tcgen05.mma and commits of every stage;
-//   warp 2     activation producer: TMA-loads the fp16 activation tile (128-byte swizzle) of each
-//              K stage, exactly the MMA's N rows, in boxes of 128, 64, 32 and 16 rows;
-//   warps 3-18 dequantize, in four groups of four warps taking the K stages round-robin (group g
-//              owns A stage g). A warp may only access its TMEM lane quadrant (warp % 4), so the
-//              four warps of a group cover the tile's 128 rows, one row per thread: the thread
-//              reads its row's quants and scales of the stage from shared memory, forms the 64
-//              fp16 weights (exact small-integer quants, one fp16 FMA with the sub-block scale
-//              and min) and stores them as 32 columns of its TMEM lane;
+//   warp 2     activation producer: TMA-loads the fp16 activation sub-tiles (128-byte swizzle)
+//              of each stage, exactly the MMA's N rows, in boxes of 128, 64, 32 and 16 rows;
+//   warps 3-18 dequantize, in four groups of four warps taking the 64-k sub-tiles round-robin.
+//              A warp may only access its TMEM lane quadrant (warp % 4), so the four warps of a
+//              group cover the tile's 128 rows, one row per thread: the thread reads its row's
+//              quants and scales of the sub-tile from shared memory, forms the 64 fp16 weights
+//              (exact small-integer quants, one fp16 FMA with the sub-block scale and min) and
+//              stores them as 32 columns of its TMEM lane;
 //   warps 19-22 epilogue: read the accumulator from TMEM (tcgen05.ld), one warp per lane
 //              quadrant, and release its buffer to the MMA.
 // Every mbarrier wait is bounded (tc::mbar_wait): on a timeout the CTA raises error bit 2 and
@@ -42,7 +45,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BK = 64;
+constexpr int BM = 128, BK = 64;  // BK: K of one 128-byte swizzled sub-tile (64 fp16)
+#ifndef GEMM_SUB
+#define GEMM_SUB 2
+#endif
+constexpr int SUB = GEMM_SUB;  // sub-tiles per pipeline stage: 8 MMAs between a wait and a commit
+constexpr int SK = SUB * BK;   // K of one pipeline stage
 constexpr int kDeqWarps = 16;
 constexpr int kDeqGroups = 4;  // groups of four warps (one per TMEM lane quadrant)
 constexpr int kFirstDeq = 3;   // warps 0-2: weight producer, MMA, activation producer
@@ -52,14 +60,14 @@ constexpr int kThreads = (kFirstDeq + kDeqWarps + kEpiWarps) * 32;  // 736
 #ifndef GEMM_BN
 #define GEMM_BN 192
 #endif
-// Tensor memory: two accumulators of BN fp32 columns, then the A stages (64 k of fp16 = 32 columns)
-// in the columns left over.
+// Tensor memory: two accumulators of BN fp32 columns, then the A stages (SK of fp16 = SK / 2
+// columns) in the columns left over.
 constexpr int ACC_COLS = GEMM_BN;
-constexpr int A_COLS = BK / 2;
+constexpr int A_COLS = SK / 2;
 constexpr int A_COL0 = 2 * ACC_COLS;
 constexpr int TMEM_COLS = 512;
 #ifndef GEMM_ASTAGES
-#define GEMM_ASTAGES ((TMEM_COLS - 2 * GEMM_BN) / (BK / 2) < 8 ? (TMEM_COLS - 2 * GEMM_BN) / (BK / 2) : 8)
+#define GEMM_ASTAGES ((TMEM_COLS - 2 * GEMM_BN) / A_COLS < 8 ? (TMEM_COLS - 2 * GEMM_BN) / A_COLS : 8)
 #endif
 constexpr int A_STAGES = GEMM_ASTAGES;
 static_assert(A_COL0 + A_STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
@@ -70,7 +78,8 @@ struct Cfg {
   static constexpr int RAWS = 4;                         // K units in flight
   // Token tile (MMA N at most): 192 tokens.
   static constexpr int BN = GEMM_BN;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int SUB_BYTES = BN * BK * 2;  // one 64-k sub-tile
+  static constexpr int B_BYTES = SUB * SUB_BYTES;
   // activation stages in shared memory, one per A stage in tensor memory
   static constexpr int B_STAGES = A_STAGES;
   static constexpr int OFF_B = 0;
@@ -225,7 +234,11 @@ __device__ __forceinline__ int item_count(const GemmArgs& p) {
   return tiles * p.m_tiles;
 }
 
-template <int FMT, bool GATEUP>
+// CS = 1, or 2 for a cluster of two CTAs that take adjacent weight slices of the same token tile
+// (items 2c + k G and 2c + 1 + k G, the weight slices fastest and their count even): each loads
+// half of every activation stage and multicasts it to both, and each MMA commit releases the stage
+// in both CTAs, so the activation tile crosses L2 once per pair.
+template <int FMT, bool GATEUP, int CS>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap16,
                                                                       const __grid_constant__ CUtensorMap tmap32,
                                                                       const __grid_constant__ CUtensorMap tmap64,
@@ -236,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int UK = unit_k(FMT), UB = unit_bytes(FMT), RAWS = C::RAWS, BS = C::B_STAGES;
-  constexpr int kpu = UK / BK;  // K stages per raw unit: Q2_K four, Q8_0 two
-  const int n_kb = p.k / UK, n_stages = p.k / BK;
+  constexpr int kpu = UK / BK;  // 64-k sub-tiles per raw unit: Q2_K four, Q8_0 two
+  const int n_kb = p.k / UK, n_stages = p.k / SK, n_subs = p.k / BK;
   const int n_items = item_count<C::BN>(p);
   // gate/up: 64 gate rows then the 64 up rows of features 64 mt .. 64 mt + 63; down: 128 rows of d
   const uint32_t raw_copy = GATEUP ? 4 * UB : 8 * UB;
@@ -258,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) {
-      mbar_init(&b.full[i], kDeqWarps / kDeqGroups + 1);  // the four warps of one dequant group + TMA
-      mbar_init(&b.empty[i], 1);
+      mbar_init(&b.full[i], SUB * (kDeqWarps / kDeqGroups) + 1);  // four warps per sub-tile + TMA
+      mbar_init(&b.empty[i], CS);                         // the MMA commit of every CTA of the cluster
     }
     for (int r = 0; r < RAWS; ++r) {
       mbar_init(&b.raw_full[r], 1);
@@ -277,9 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (CS > 1)
+    cluster_sync();  // the peer's barriers are initialized before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+  constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ weight producer
@@ -314,14 +332,29 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
           const int sb = gs % BS;
           if (!mbar_wait(&b.empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
-          // exactly the MMA's N rows: 128-row boxes, then at most one box each of 64, 32 and 16
+          // exactly the MMA's N rows of each sub-tile (all of them land in this CTA), of which
+          // this CTA loads its share [lo, hi): 128-row boxes, then at most one box each of 64, 32
+          // and 16 rows
           const int rows = t.n;
-          mbar_expect_tx(&b.full[sb], rows * BK * 2);
-          int r = 0;
-          for (; rows - r >= 128; r += 128) tma_load_2d(bdst + r * BK * 2, &tmap128, sB * BK, t.row0 + r, &b.full[sb]);
-          if (rows - r >= 64) { tma_load_2d(bdst + r * BK * 2, &tmap64, sB * BK, t.row0 + r, &b.full[sb]); r += 64; }
-          if (rows - r >= 32) { tma_load_2d(bdst + r * BK * 2, &tmap32, sB * BK, t.row0 + r, &b.full[sb]); r += 32; }
-          if (rows - r >= 16) tma_load_2d(bdst + r * BK * 2, &tmap16, sB * BK, t.row0 + r, &b.full[sb]);
+          mbar_expect_tx(&b.full[sb], SUB * rows * BK * 2);
+          const int half = (rows / 32) * 16;
+          const int lo = CS > 1 && rank ? half : 0, hi = CS > 1 && !rank ? half : rows;
+#pragma unroll
+          for (int j = 0; j < SUB; ++j) {
+            unsigned char* sdst = bdst + j * C::SUB_BYTES;
+            const int x = (sB * SUB + j) * BK;
+            auto load = [&](const CUtensorMap* map, int r) {
+              if (CS > 1)
+                tma_load_2d_mc(sdst + r * BK * 2, map, x, t.row0 + r, &b.full[sb], kMask);
+              else
+                tma_load_2d(sdst + r * BK * 2, map, x, t.row0 + r, &b.full[sb]);
+            };
+            int r = lo;
+            for (; hi - r >= 128; r += 128) load(&tmap128, r);
+            if (hi - r >= 64) { load(&tmap64, r); r += 64; }
+            if (hi - r >= 32) { load(&tmap32, r); r += 32; }
+            if (hi - r >= 16) load(&tmap16, r);
+          }
         }
       }
       for (uint32_t k = gs > (uint32_t)BS ? gs - BS : 0; k < gs; ++k)
@@ -349,41 +382,48 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
         tc_fence_after();
         const uint32_t ta = tmem + (uint32_t)(A_COL0 + st * A_COLS);
-        const uint64_t bd = sw128_desc(su32(smem + C::OFF_B + st * C::B_BYTES));
+        const uint32_t bsm = su32(smem + C::OFF_B + st * C::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
-          tc_mma_f16_ts_elect(acc, ta + 8 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-        tc_commit_elect(&b.empty[st]);
+        for (int kk = 0; kk < SK / 16; ++kk)  // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
+          tc_mma_f16_ts_elect(acc, ta + 8 * kk, sw128_desc(bsm + (kk / 4) * C::SUB_BYTES) + 2 * (kk % 4), idesc,
+                              (s | kk) != 0);
+        if (CS > 1)
+          tc_commit_mc_elect(&b.empty[st], kMask);
+        else
+          tc_commit_elect(&b.empty[st]);
       }
       if (!ok) break;
       tc_commit_elect(&b.acc_full[buf]);
     }
-    // After an abort, the MMAs already issued must finish before TMEM is freed: the commit of the
-    // last issued stage (stage gs - 1) arrives only once all of them have completed.
-    if (*abort_flag && gs > 0 && lane == 0) bounded_try(&b.empty[(gs - 1) % BS], ((gs - 1) / BS) & 1, limit);
+    // The MMAs already issued must finish before TMEM is freed (after an abort), and in a cluster
+    // every commit of both CTAs must have reached its barriers before either CTA exits: the
+    // last stage's empty phase completes only then.
+    if ((*abort_flag || CS > 1) && gs > 0 && lane == 0)
+      bounded_try(&b.empty[(gs - 1) % BS], ((gs - 1) / BS) & 1, limit);
     __syncwarp();
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
-    // Four groups of four warps take the CTA's K stages round-robin: group g dequantizes the
-    // stages gs = g (mod 4), each into A stage gs (mod A_STAGES). Warp w accesses TMEM lanes
-    // 32 (w % 4) .. + 31, and a group's four consecutive warps cover all four quadrants; a thread
-    // owns tile row = its lane.
+    // Four groups of four warps take the CTA's 64-k sub-tiles round-robin: group g dequantizes the
+    // sub-tiles gs = g (mod 4), sub-tile gs % SUB of pipeline stage gs / SUB. Warp w accesses TMEM
+    // lanes 32 (w % 4) .. + 31, and a group's four consecutive warps cover all four quadrants; a
+    // thread owns tile row = its lane.
     const int dw = warp - kFirstDeq;
     const int grp = dw / (kDeqWarps / kDeqGroups);
     const int quad = warp & 3;
     const int row = 32 * quad + lane;                      // tile row = TMEM lane
     const int rho = row & 15, g = rho & 7, ah = rho >> 3;  // row inside its 16-row unit
     const uint32_t t_q = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)A_COL0;
-    uint32_t gs0 = 0;  // stages of the CTA's earlier items
+    uint32_t gs0 = 0;  // sub-tiles of the CTA's earlier items
     for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
       bool ok = true;
-      for (int s = (grp - (int)(gs0 % kDeqGroups) + kDeqGroups) % kDeqGroups; s < n_stages; s += kDeqGroups) {
+      for (int s = (grp - (int)(gs0 % kDeqGroups) + kDeqGroups) % kDeqGroups; s < n_subs; s += kDeqGroups) {
         const uint32_t gs = gs0 + s;
-        const uint32_t gu = gs / kpu;  // the raw units follow the stages
+        const uint32_t gu = gs / kpu;  // the raw units follow the sub-tiles
         const int rs = gu % RAWS, su = gs % kpu;
         if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3, limit)) { ok = false; break; }
-        const int sa = gs % A_STAGES;
-        if (!mbar_wait(&b.empty[sa], ((gs / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
+        const uint32_t ps = gs / SUB;  // pipeline stage
+        const int sa = ps % A_STAGES;
+        if (!mbar_wait(&b.empty[sa], ((ps / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
         tc_fence_after();
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES) + (row >> 4) * UB;
         uint32_t v[32];
@@ -398,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
           else
             deq_q80_row<0>(unit, g, ah, v);
         }
-        tmem_st32(t_q + (uint32_t)(sa * A_COLS), v);
+        tmem_st32(t_q + (uint32_t)(sa * A_COLS + (gs % SUB) * (BK / 2)), v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -409,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
       }
       if (!ok) break;
-      gs0 += n_stages;
+      gs0 += n_subs;
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -476,48 +516,110 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CS > 1)
+    cluster_sync();  // no copy or commit of either CTA still targets the other's shared memory
+  else
+    __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int FMT, bool GATEUP>
-cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, dim3 grid, cudaStream_t s) {
-  expert_gemm_tc_kernel<FMT, GATEUP><<<grid, kThreads, Cfg<FMT>::SMEM_BYTES, s>>>(tm.r16, tm.r32, tm.r64, tm.r128, p);
-  return cudaGetLastError();
+template <int FMT, bool GATEUP, int CS>
+cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<FMT>::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CS > 1 ? 1 : 0;  // a plain launch without clusters
+  return cudaLaunchKernelEx(&cfg, expert_gemm_tc_kernel<FMT, GATEUP, CS>, tm.r16, tm.r32, tm.r64, tm.r128, p);
+}
+
+// Clusters of CS CTAs that can be resident at once (0 if none).
+template <int FMT, bool GATEUP, int CS>
+int max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * CS);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<FMT>::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_tc_kernel<FMT, GATEUP, CS>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int FMT, bool GATEUP, int CS>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<FMT>::SMEM_BYTES);
 }
 
 template <int FMT, bool GATEUP>
-cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<FMT>::SMEM_BYTES);
+cudaError_t prepare_fmt(int* pairs) {
+  cudaError_t e = prepare_one<FMT, GATEUP, 1>();
+  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 2>();
+  *pairs = e == cudaSuccess ? max_clusters<FMT, GATEUP, 2>() : 0;
+  return e;
 }
+
+// Per device: resident clusters of two for each (format, gate/up or down) kernel.
+int g_pairs[64][4];
 
 }  // namespace
 
 int gemm_tile_n(int fmt) { return fmt == FMT_Q2_K ? Cfg<FMT_Q2_K>::BN : Cfg<FMT_Q8_0>::BN; }
 
 cudaError_t gemm_prepare() {
-  cudaError_t e = prepare_one<FMT_Q2_K, true>();
-  if (e == cudaSuccess) e = prepare_one<FMT_Q2_K, false>();
-  if (e == cudaSuccess) e = prepare_one<FMT_Q8_0, true>();
-  if (e == cudaSuccess) e = prepare_one<FMT_Q8_0, false>();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int scratch[4];
+  int* pairs = (dev >= 0 && dev < 64) ? g_pairs[dev] : scratch;
+  cudaError_t e = prepare_fmt<FMT_Q2_K, true>(&pairs[0]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q2_K, false>(&pairs[1]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, true>(&pairs[2]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, false>(&pairs[3]);
   return e;
 }
 
 // Persistent launch: one CTA per SM (at most), each looping over the (token tile, weight slice)
-// items; n_tiles bounds the token tiles (the routed count itself is read on the device).
+// items; n_tiles bounds the token tiles (the routed count itself is read on the device). With an
+// even number of weight slices, the CTAs run in clusters of two that share the activation loads.
 cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& args, int m_tiles, int n_tiles,
                         cudaStream_t s) {
   static int n_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !n_sm[dev]) cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
-  const int sms = (dev >= 0 && dev < 64 && n_sm[dev] > 0) ? n_sm[dev] : 152;
+  const bool known = dev >= 0 && dev < 64;
+  if (known && !n_sm[dev]) cudaDeviceGetAttribute(&n_sm[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = (known && n_sm[dev] > 0) ? n_sm[dev] : 152;
   GemmArgs p = args;
   p.m_tiles = m_tiles;
-  const dim3 grid(std::max(1, std::min(sms, m_tiles * n_tiles)));
-  if (fmt == FMT_Q2_K) return gateup ? launch_one<FMT_Q2_K, true>(tm, p, grid, s) : launch_one<FMT_Q2_K, false>(tm, p, grid, s);
-  return gateup ? launch_one<FMT_Q8_0, true>(tm, p, grid, s) : launch_one<FMT_Q8_0, false>(tm, p, grid, s);
+  const int items = m_tiles * n_tiles;
+  const int pairs = known ? g_pairs[dev][(fmt == FMT_Q2_K ? 0 : 2) + (gateup ? 0 : 1)] : 0;
+  if (m_tiles % 2 == 0 && pairs > 0) {
+    const int grid = 2 * std::max(1, std::min(pairs, items / 2));
+    if (fmt == FMT_Q2_K)
+      return gateup ? launch_one<FMT_Q2_K, true, 2>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, 2>(tm, p, grid, s);
+    return gateup ? launch_one<FMT_Q8_0, true, 2>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, 2>(tm, p, grid, s);
+  }
+  const int grid = std::max(1, std::min(sms, items));
+  if (fmt == FMT_Q2_K)
+    return gateup ? launch_one<FMT_Q2_K, true, 1>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, 1>(tm, p, grid, s);
+  return gateup ? launch_one<FMT_Q8_0, true, 1>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, 1>(tm, p, grid, s);
 }
 
 // fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x box_rows rows
