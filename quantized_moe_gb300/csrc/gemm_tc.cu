@@ -9,12 +9,12 @@
 // warps write it into tensor memory (tcgen05.st) and the MMA reads A from there and only the
 // activation tile (B) from shared memory. Tensor memory holds two fp32 accumulators of 192
 // columns (the epilogue of one item overlaps the main loop of the next) and two pipeline stages of
-// A (128 k = 64 columns each); shared memory holds two activation stages and the packed weight
-// units. A pipeline stage is two 64-k sub-tiles (one 128-byte swizzle span each). It has one full
-// barrier, completed by the two dequant groups that wrote its A sub-tiles and by the activation
-// TMA, and one empty barrier, completed by the MMA commit: the MMA thread makes one wait and one
-// commit per eight MMAs (the loop of barrier operations, more than the tensor pipe, bounds the
-// stage rate, so a stage carries as much MMA work as tensor memory allows).
+// A (128 k = 64 columns each); shared memory holds three activation stages and the packed weight
+// units. A pipeline stage is two 64-k sub-tiles (one 128-byte swizzle span each) and carries eight
+// MMAs per barrier wait and commit: the MMA thread's loop of barrier operations, more than the
+// tensor pipe, bounds the stage rate. The A stages have their own full barrier (the two dequant
+// groups that wrote the sub-tiles) and empty barrier (MMA commit), and so have the activation
+// stages (TMA bytes; MMA commit), so that the activation ring can run a stage further ahead.
 // With an even number of weight slices the CTAs run in clusters of two on adjacent slices of the
 // same token tile and each loads half of every activation stage, multicast to both.
 // Warp roles (23 warps):
@@ -81,12 +81,17 @@ struct Cfg {
   static constexpr int SUB_BYTES = BN * BK * 2;  // one 64-k sub-tile
   static constexpr int B_BYTES = SUB * SUB_BYTES;
   // activation stages in shared memory, one per A stage in tensor memory
-  static constexpr int B_STAGES = A_STAGES;
+#ifndef GEMM_BSTAGES
+#define GEMM_BSTAGES 3
+#endif
+  // activation stages: more than the A stages, so that the TMA of a stage is issued well before
+  // the MMA needs it (an L2 read under load takes around a thousand cycles)
+  static constexpr int B_STAGES = GEMM_BSTAGES;
   static constexpr int OFF_B = 0;
   static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
   static_assert(BN <= 256 && BN % 16 == 0, "token tile");
   static constexpr int OFF_BAR = OFF_RAW + RAWS * RAW_BYTES;
-  static constexpr int N_BARS = 2 * A_STAGES + 2 * RAWS + 4;
+  static constexpr int N_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * RAWS + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_GBUF = (OFF_MISC + 16 + 15) / 16 * 16;
   // gate/up epilogue: two parities x (8 columns of g + 8 columns of u) x 64 features fp32, then the
@@ -97,8 +102,10 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t* full;       // [A_STAGES] the dequant group's four warps + activation TMA (with its bytes) -> MMA
-  uint64_t* empty;      // [A_STAGES] MMA commit -> dequant group and activation producer
+  uint64_t* a_full;     // [A_STAGES] the dequant groups' warps -> MMA
+  uint64_t* a_empty;    // [A_STAGES] MMA commit -> dequant groups
+  uint64_t* b_full;     // [B_STAGES] activation TMA (with its bytes) -> MMA
+  uint64_t* b_empty;    // [B_STAGES] MMA commits of every CTA of the cluster -> activation producer
   uint64_t* raw_full;   // [RAWS] weight bulk copy -> dequant
   uint64_t* raw_empty;  // [RAWS] dequant -> producer
   uint64_t* acc_full;   // [2] MMA -> epilogue
@@ -258,9 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
   Bars b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  b.full = bars;
-  b.empty = b.full + A_STAGES;
-  b.raw_full = b.empty + A_STAGES;
+  b.a_full = bars;
+  b.a_empty = b.a_full + A_STAGES;
+  b.b_full = b.a_empty + A_STAGES;
+  b.b_empty = b.b_full + BS;
+  b.raw_full = b.b_empty + BS;
   b.raw_empty = b.raw_full + RAWS;
   b.acc_full = b.raw_empty + RAWS;  // [2]
   b.acc_empty = b.acc_full + 2;     // [2]
@@ -271,8 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) {
-      mbar_init(&b.full[i], SUB * (kDeqWarps / kDeqGroups) + 1);  // four warps per sub-tile + TMA
-      mbar_init(&b.empty[i], CS);                         // the MMA commit of every CTA of the cluster
+      mbar_init(&b.a_full[i], SUB * (kDeqWarps / kDeqGroups));  // four warps per sub-tile
+      mbar_init(&b.a_empty[i], 1);
+    }
+    for (int i = 0; i < BS; ++i) {
+      mbar_init(&b.b_full[i], 1);
+      mbar_init(&b.b_empty[i], CS);  // the MMA commit of every CTA of the cluster
     }
     for (int r = 0; r < RAWS; ++r) {
       mbar_init(&b.raw_full[r], 1);
@@ -330,13 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         const Item t = item_of<C::BN>(p, it);
         for (int sB = 0; sB < n_stages; ++sB, ++gs) {
           const int sb = gs % BS;
-          if (!mbar_wait(&b.empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
+          if (!mbar_wait(&b.b_empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
           unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
           // exactly the MMA's N rows of each sub-tile (all of them land in this CTA), of which
           // this CTA loads its share [lo, hi): 128-row boxes, then at most one box each of 64, 32
           // and 16 rows
           const int rows = t.n;
-          mbar_expect_tx(&b.full[sb], SUB * rows * BK * 2);
+          mbar_expect_tx(&b.b_full[sb], SUB * rows * BK * 2);
           const int half = (rows / 32) * 16;
           const int lo = CS > 1 && rank ? half : 0, hi = CS > 1 && !rank ? half : rows;
 #pragma unroll
@@ -345,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
             const int x = (sB * SUB + j) * BK;
             auto load = [&](const CUtensorMap* map, int r) {
               if (CS > 1)
-                tma_load_2d_mc(sdst + r * BK * 2, map, x, t.row0 + r, &b.full[sb], kMask);
+                tma_load_2d_mc(sdst + r * BK * 2, map, x, t.row0 + r, &b.b_full[sb], kMask);
               else
-                tma_load_2d(sdst + r * BK * 2, map, x, t.row0 + r, &b.full[sb]);
+                tma_load_2d(sdst + r * BK * 2, map, x, t.row0 + r, &b.b_full[sb]);
             };
             int r = lo;
             for (; hi - r >= 128; r += 128) load(&tmap128, r);
@@ -358,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         }
       }
       for (uint32_t k = gs > (uint32_t)BS ? gs - BS : 0; k < gs; ++k)
-        bounded_try(&b.full[k % BS], (k / BS) & 1, limit);
+        bounded_try(&b.b_full[k % BS], (k / BS) & 1, limit);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -376,21 +389,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
       bool ok = true;
       for (int s = 0; s < n_stages; ++s, ++gs) {
         const int st = gs % A_STAGES;
-        if (!warp_wait(&b.full[st], (gs / A_STAGES) & 1, abort_flag, p.err, 7, limit)) {
+        const int sb = gs % BS;
+        if (!warp_wait(&b.b_full[sb], (gs / BS) & 1, abort_flag, p.err, 7, limit) ||
+            !warp_wait(&b.a_full[st], (gs / A_STAGES) & 1, abort_flag, p.err, 7, limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t ta = tmem + (uint32_t)(A_COL0 + st * A_COLS);
-        const uint32_t bsm = su32(smem + C::OFF_B + st * C::B_BYTES);
+        const uint32_t bsm = su32(smem + C::OFF_B + sb * C::B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < SK / 16; ++kk)  // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
           tc_mma_f16_ts_elect(acc, ta + 8 * kk, sw128_desc(bsm + (kk / 4) * C::SUB_BYTES) + 2 * (kk % 4), idesc,
                               (s | kk) != 0);
         if (CS > 1)
-          tc_commit_mc_elect(&b.empty[st], kMask);
+          tc_commit_mc_elect(&b.b_empty[sb], kMask);
         else
-          tc_commit_elect(&b.empty[st]);
+          tc_commit_elect(&b.b_empty[sb]);
+        tc_commit_elect(&b.a_empty[st]);
       }
       if (!ok) break;
       tc_commit_elect(&b.acc_full[buf]);
@@ -399,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     // every commit of both CTAs must have reached its barriers before either CTA exits: the
     // last stage's empty phase completes only then.
     if ((*abort_flag || CS > 1) && gs > 0 && lane == 0)
-      bounded_try(&b.empty[(gs - 1) % BS], ((gs - 1) / BS) & 1, limit);
+      bounded_try(&b.b_empty[(gs - 1) % BS], ((gs - 1) / BS) & 1, limit);
     __syncwarp();
   } else if (warp < kFirstDeq + kDeqWarps) {
     // ------------------------------------------------------------------ dequant
@@ -423,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         if (!mbar_wait(&b.raw_full[rs], (gu / RAWS) & 1, abort_flag, p.err, 3, limit)) { ok = false; break; }
         const uint32_t ps = gs / SUB;  // pipeline stage
         const int sa = ps % A_STAGES;
-        if (!mbar_wait(&b.empty[sa], ((ps / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
+        if (!mbar_wait(&b.a_empty[sa], ((ps / A_STAGES) & 1) ^ 1, abort_flag, p.err, 4, limit)) { ok = false; break; }
         tc_fence_after();
         const uint32_t unit = su32(smem + C::OFF_RAW + rs * C::RAW_BYTES) + (row >> 4) * UB;
         uint32_t v[32];
@@ -444,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         __syncwarp();
         if (lane == 0) {
           // (a test of the timeout path withholds one arrival: that stage never becomes full)
-          if (!(p.test_stall && blockIdx.x == 0 && gs + 1 == (uint32_t)p.test_stall)) mbar_arrive(&b.full[sa]);
+          if (!(p.test_stall && blockIdx.x == 0 && gs + 1 == (uint32_t)p.test_stall)) mbar_arrive(&b.a_full[sa]);
           mbar_arrive(&b.raw_empty[rs]);
         }
       }
