@@ -23,7 +23,8 @@
 //   warp 1     allocates TMEM; the converged warp runs the MMA loop and one elected lane issues
 //              the tcgen05.mma and commits of every stage;
 //   warp 2     activation producer: TMA-loads the fp16 activation sub-tiles (128-byte swizzle)
-//              of each stage, exactly the MMA's N rows, in boxes of 128, 64, 32 and 16 rows;
+//              of each stage, exactly the MMA's N rows, in boxes of 128, 64, 32 and 16 rows
+//              issued by parallel lanes (one thread issuing them in turn was the critical path);
 //   warps 3-18 dequantize, in four groups of four warps taking the 64-k sub-tiles round-robin.
 //              A warp may only access its TMEM lane quadrant (warp % 4), so the four warps of a
 //              group cover the tile's 128 rows, one row per thread: the thread reads its row's
@@ -75,18 +76,21 @@ static_assert(A_COL0 + A_STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
 template <int FMT>
 struct Cfg {
   static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);  // one K unit of the 128-row tile
-  static constexpr int RAWS = 4;                         // K units in flight
+#ifndef GEMM_RAWS_Q2K
+#define GEMM_RAWS_Q2K 4
+#endif
+  static constexpr int RAWS = FMT == FMT_Q2_K ? GEMM_RAWS_Q2K : 4;  // K units in flight
   // Token tile (MMA N at most): 192 tokens.
   static constexpr int BN = GEMM_BN;
   static constexpr int SUB_BYTES = BN * BK * 2;  // one 64-k sub-tile
   static constexpr int B_BYTES = SUB * SUB_BYTES;
   // activation stages in shared memory, one per A stage in tensor memory
-#ifndef GEMM_BSTAGES
-#define GEMM_BSTAGES 3
+#ifndef GEMM_BSTAGES_Q2K
+#define GEMM_BSTAGES_Q2K 3
 #endif
   // activation stages: more than the A stages, so that the TMA of a stage is issued well before
   // the MMA needs it (an L2 read under load takes around a thousand cycles)
-  static constexpr int B_STAGES = GEMM_BSTAGES;
+  static constexpr int B_STAGES = FMT == FMT_Q2_K ? GEMM_BSTAGES_Q2K : 3;
   static constexpr int OFF_B = 0;
   static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
   static_assert(BN <= 256 && BN % 16 == 0, "token tile");
@@ -241,10 +245,11 @@ __device__ __forceinline__ int item_count(const GemmArgs& p) {
   return tiles * p.m_tiles;
 }
 
-// CS = 1, or 2 for a cluster of two CTAs that take adjacent weight slices of the same token tile
-// (items 2c + k G and 2c + 1 + k G, the weight slices fastest and their count even): each loads
-// half of every activation stage and multicasts it to both, and each MMA commit releases the stage
-// in both CTAs, so the activation tile crosses L2 once per pair.
+// CS = 1, or the size (2 or 4) of a cluster of CTAs that take adjacent weight slices of the same
+// token tile (items CS c + r + k G, r < CS, the weight slices fastest and their count a multiple
+// of CS): each loads its share of the rows of every activation stage and multicasts it to all,
+// and each MMA commit releases the stage in all of them, so the activation tile crosses L2 once
+// per cluster.
 template <int FMT, bool GATEUP, int CS>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap16,
                                                                       const __grid_constant__ CUtensorMap tmap32,
@@ -310,6 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+  if (warp == 2 && lane == 0) {  // the activation producer's descriptors, ahead of its first loads
+    tmap_prefetch(&tmap16);
+    tmap_prefetch(&tmap32);
+    tmap_prefetch(&tmap64);
+    tmap_prefetch(&tmap128);
+  }
   constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
 
   if (warp == 0) {
@@ -337,42 +348,47 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ activation producer
-    if (lane == 0) {
-      uint32_t gs = 0;  // stages issued over all items
-      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
-        const Item t = item_of<C::BN>(p, it);
-        for (int sB = 0; sB < n_stages; ++sB, ++gs) {
-          const int sb = gs % BS;
-          if (!mbar_wait(&b.b_empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
-          unsigned char* bdst = smem + C::OFF_B + sb * C::B_BYTES;
-          // exactly the MMA's N rows of each sub-tile (all of them land in this CTA), of which
-          // this CTA loads its share [lo, hi): 128-row boxes, then at most one box each of 64, 32
-          // and 16 rows
-          const int rows = t.n;
-          mbar_expect_tx(&b.b_full[sb], SUB * rows * BK * 2);
-          const int half = (rows / 32) * 16;
-          const int lo = CS > 1 && rank ? half : 0, hi = CS > 1 && !rank ? half : rows;
-#pragma unroll
-          for (int j = 0; j < SUB; ++j) {
-            unsigned char* sdst = bdst + j * C::SUB_BYTES;
-            const int x = (sB * SUB + j) * BK;
-            auto load = [&](const CUtensorMap* map, int r) {
-              if (CS > 1)
-                tma_load_2d_mc(sdst + r * BK * 2, map, x, t.row0 + r, &b.b_full[sb], kMask);
-              else
-                tma_load_2d(sdst + r * BK * 2, map, x, t.row0 + r, &b.b_full[sb]);
-            };
-            int r = lo;
-            for (; hi - r >= 128; r += 128) load(&tmap128, r);
-            if (hi - r >= 64) { load(&tmap64, r); r += 64; }
-            if (hi - r >= 32) { load(&tmap32, r); r += 32; }
-            if (hi - r >= 16) load(&tmap16, r);
-          }
+    // The warp waits for a free stage together; lane 0 announces the stage's bytes and lane 8j + q
+    // issues box q of sub-tile j: the CTA's rows [lo, hi) of the MMA's N rows as boxes of 128,
+    // 128, 64, 32 and 16 rows (those the length needs), so that all of a stage's loads go out in
+    // one instruction instead of one after another from a single thread.
+    uint32_t gs = 0;  // stages issued over all items
+    const int j = lane >> 3, q = lane & 7;
+    for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x) {
+      const Item t = item_of<C::BN>(p, it);
+      const int rows = t.n;  // all of them land in this CTA
+      const int lo = 16 * ((rows / 16) * rank / CS), hi = 16 * ((rows / 16) * (rank + 1) / CS);
+      const int len = hi - lo, n128 = len / 128, rem = len - 128 * n128;
+      int r = -1;
+      const CUtensorMap* map = &tmap16;
+      if (q < 2) {
+        if (q < n128) r = lo + 128 * q, map = &tmap128;
+      } else if (q == 2) {
+        if (rem & 64) r = lo + 128 * n128, map = &tmap64;
+      } else if (q == 3) {
+        if (rem & 32) r = lo + 128 * n128 + (rem & 64), map = &tmap32;
+      } else if (q == 4) {
+        if (rem & 16) r = lo + 128 * n128 + (rem & 96), map = &tmap16;
+      }
+      const bool issue = j < SUB && r >= 0;
+      for (int sB = 0; sB < n_stages; ++sB, ++gs) {
+        const int sb = gs % BS;
+        if (!warp_wait(&b.b_empty[sb], ((gs / BS) & 1) ^ 1, abort_flag, p.err, 2, limit)) break;
+        if (lane == 0) mbar_expect_tx(&b.b_full[sb], SUB * rows * BK * 2);
+        if (issue) {
+          unsigned char* dst = smem + C::OFF_B + sb * C::B_BYTES + j * C::SUB_BYTES + r * BK * 2;
+          const int x = (sB * SUB + j) * BK;
+          if (CS > 1)
+            tma_load_2d_mc(dst, map, x, t.row0 + r, &b.b_full[sb], kMask);
+          else
+            tma_load_2d(dst, map, x, t.row0 + r, &b.b_full[sb]);
         }
       }
+    }
+    if (lane == 0)
       for (uint32_t k = gs > (uint32_t)BS ? gs - BS : 0; k < gs; ++k)
         bounded_try(&b.b_full[k % BS], (k / BS) & 1, limit);
-    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop and polls the barriers; one elected lane issues.
@@ -585,15 +601,17 @@ cudaError_t prepare_one() {
 }
 
 template <int FMT, bool GATEUP>
-cudaError_t prepare_fmt(int* pairs) {
+cudaError_t prepare_fmt(int* pairs, int* quads) {
   cudaError_t e = prepare_one<FMT, GATEUP, 1>();
   if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 2>();
+  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 4>();
   *pairs = e == cudaSuccess ? max_clusters<FMT, GATEUP, 2>() : 0;
+  *quads = e == cudaSuccess ? max_clusters<FMT, GATEUP, 4>() : 0;
   return e;
 }
 
-// Per device: resident clusters of two for each (format, gate/up or down) kernel.
-int g_pairs[64][4];
+// Per device: resident clusters of two and of four for each (format, gate/up or down) kernel.
+int g_pairs[64][4], g_quads[64][4];
 
 }  // namespace
 
@@ -602,18 +620,28 @@ int gemm_tile_n(int fmt) { return fmt == FMT_Q2_K ? Cfg<FMT_Q2_K>::BN : Cfg<FMT_
 cudaError_t gemm_prepare() {
   int dev = 0;
   cudaGetDevice(&dev);
-  int scratch[4];
+  int scratch[8];
   int* pairs = (dev >= 0 && dev < 64) ? g_pairs[dev] : scratch;
-  cudaError_t e = prepare_fmt<FMT_Q2_K, true>(&pairs[0]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q2_K, false>(&pairs[1]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, true>(&pairs[2]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, false>(&pairs[3]);
+  int* quads = (dev >= 0 && dev < 64) ? g_quads[dev] : scratch + 4;
+  cudaError_t e = prepare_fmt<FMT_Q2_K, true>(&pairs[0], &quads[0]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q2_K, false>(&pairs[1], &quads[1]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, true>(&pairs[2], &quads[2]);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, false>(&pairs[3], &quads[3]);
   return e;
 }
 
+template <int CS>
+cudaError_t launch_cs(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int grid, cudaStream_t s) {
+  if (fmt == FMT_Q2_K)
+    return gateup ? launch_one<FMT_Q2_K, true, CS>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, CS>(tm, p, grid, s);
+  return gateup ? launch_one<FMT_Q8_0, true, CS>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, CS>(tm, p, grid, s);
+}
+
 // Persistent launch: one CTA per SM (at most), each looping over the (token tile, weight slice)
-// items; n_tiles bounds the token tiles (the routed count itself is read on the device). With an
-// even number of weight slices, the CTAs run in clusters of two that share the activation loads.
+// items; n_tiles bounds the token tiles (the routed count itself is read on the device). When the
+// weight slices divide evenly, the CTAs run in clusters that share the activation loads: of four
+// for the dense (shared expert) GEMMs, of two for the routed ones (measured: clusters of four leave
+// more SMs idle than the routed GEMMs gain from the smaller activation traffic).
 cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& args, int m_tiles, int n_tiles,
                         cudaStream_t s) {
   static int n_sm[64] = {};
@@ -625,17 +653,13 @@ cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs&
   GemmArgs p = args;
   p.m_tiles = m_tiles;
   const int items = m_tiles * n_tiles;
-  const int pairs = known ? g_pairs[dev][(fmt == FMT_Q2_K ? 0 : 2) + (gateup ? 0 : 1)] : 0;
-  if (m_tiles % 2 == 0 && pairs > 0) {
-    const int grid = 2 * std::max(1, std::min(pairs, items / 2));
-    if (fmt == FMT_Q2_K)
-      return gateup ? launch_one<FMT_Q2_K, true, 2>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, 2>(tm, p, grid, s);
-    return gateup ? launch_one<FMT_Q8_0, true, 2>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, 2>(tm, p, grid, s);
-  }
-  const int grid = std::max(1, std::min(sms, items));
-  if (fmt == FMT_Q2_K)
-    return gateup ? launch_one<FMT_Q2_K, true, 1>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, 1>(tm, p, grid, s);
-  return gateup ? launch_one<FMT_Q8_0, true, 1>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, 1>(tm, p, grid, s);
+  const int k = (fmt == FMT_Q2_K ? 0 : 2) + (gateup ? 0 : 1);
+  const int quads = known ? g_quads[dev][k] : 0, pairs = known ? g_pairs[dev][k] : 0;
+  if (!args.tiles && m_tiles % 4 == 0 && quads > 0)
+    return launch_cs<4>(fmt, gateup, tm, p, 4 * std::max(1, std::min(quads, items / 4)), s);
+  if (m_tiles % 2 == 0 && pairs > 0)
+    return launch_cs<2>(fmt, gateup, tm, p, 2 * std::max(1, std::min(pairs, items / 2)), s);
+  return launch_cs<1>(fmt, gateup, tm, p, std::max(1, std::min(sms, items)), s);
 }
 
 // fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x box_rows rows

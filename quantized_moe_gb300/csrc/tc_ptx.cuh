@@ -84,6 +84,11 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map
       : "memory");
 }
 
+// Brings a tensor map's descriptor into the TMA unit's cache before its first use.
+__device__ __forceinline__ void tmap_prefetch(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
