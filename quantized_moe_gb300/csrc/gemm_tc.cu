@@ -414,15 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         tc_fence_after();
         const uint32_t ta = tmem + (uint32_t)(A_COL0 + st * A_COLS);
         const uint32_t bsm = su32(smem + C::OFF_B + sb * C::B_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < SK / 16; ++kk)  // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
-          tc_mma_f16_ts_elect(acc, ta + 8 * kk, sw128_desc(bsm + (kk / 4) * C::SUB_BYTES) + 2 * (kk % 4), idesc,
-                              (s | kk) != 0);
-        if (CS > 1)
-          tc_commit_mc_elect(&b.b_empty[sb], kMask);
-        else
-          tc_commit_elect(&b.b_empty[sb]);
-        tc_commit_elect(&b.a_empty[st]);
+        // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of a B sub-tile
+        static_assert(SUB == 2, "the stage's MMAs are issued as one block of eight");
+        tc_mma8_ts_elect(acc, ta, sw128_desc(bsm), sw128_desc(bsm + C::SUB_BYTES), idesc, s != 0);
+        tc_commit2_elect(&b.b_empty[sb], CS > 1 ? kMask : 0, &b.a_empty[st]);
       }
       if (!ok) break;
       tc_commit_elect(&b.acc_full[buf]);
