@@ -145,6 +145,48 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
+// Eight MMAs of one 128-k stage (A in tensor memory, 64 columns from a_tmem; B as two 64-k
+// sub-tiles with descriptors b0 and b1, each advanced 32 bytes per 16 k), issued by one elected
+// lane of the converged warp: one elect and no compiler ordering between the eight. The first
+// MMA accumulates into D only if accumulate != 0; the other seven always do.
+__device__ __forceinline__ void tc_mma8_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint64_t b1,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, t, e;\n .reg .b32 a;\n .reg .b64 b;\n"
+      " setp.ne.b32 p, %5, 0;\n setp.eq.b32 t, %5, %5;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n"
+      " add.u32 a, %1, 8;\n add.u64 b, %2, 2;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      " add.u32 a, %1, 16;\n add.u64 b, %2, 4;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      " add.u32 a, %1, 24;\n add.u64 b, %2, 6;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      " add.u32 a, %1, 32;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %3, %4, t;\n"
+      " add.u32 a, %1, 40;\n add.u64 b, %3, 2;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      " add.u32 a, %1, 48;\n add.u64 b, %3, 4;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      " add.u32 a, %1, 56;\n add.u64 b, %3, 6;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The commits that release a stage: a multicast commit to the activation stage's barrier in every
+// CTA of the cluster in mask (or a plain one if mask is 0) and a commit to the local A stage's
+// barrier, issued by one elected lane.
+__device__ __forceinline__ void tc_commit2_elect(uint64_t* b_bar, uint16_t mask, uint64_t* a_bar) {
+  if (mask)
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%2];\n}\n" ::"r"(su32(b_bar)),
+        "h"(mask), "r"(su32(a_bar))
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n}\n" ::"r"(su32(b_bar)),
+        "r"(su32(a_bar))
+        : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns of the warp's TMEM lane quadrant.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
