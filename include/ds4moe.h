@@ -56,10 +56,12 @@ extern "C" {
 #define DS4MOE_ERR_UNSUPPORTED_FORMAT -2 /* format enum not Q8_0 / Q2_K, or shape not tileable; also
                                             a Q2_K super-block with |d| >= 0.0666 (more precisely,
                                             15 * 2^16 * |d| >= 65504) on a handle whose max_tokens
-                                            enables the batched path (max_tokens > 16 or
+                                            needs the batched path (max_tokens > 16 or
                                             max_tokens * top_k > 128): that path dequantizes Q2_K
-                                            weights in fp16 as q * 2^-16 times 2^16 * d * s. Decode-
-                                            only handles accept any fp16 d */
+                                            weights in fp16 as q * 2^-16 times 2^16 * d * s. Handles
+                                            with max_tokens <= 16 (and max_tokens * top_k <= 128)
+                                            accept any fp16 d: with such scales they serve every
+                                            forward on the decode path */
 #define DS4MOE_ERR_DEVICE_MISMATCH -3    /* a device pointer lives on another GPU than the handle */
 #define DS4MOE_ERR_CAPACITY -4           /* n_tokens > max_tokens given at create */
 #define DS4MOE_ERR_OOM -5                /* device allocation failed or exceeded workspace_limit */
@@ -128,7 +130,14 @@ typedef struct ds4moe_stats {
 typedef struct ds4moe_handle ds4moe_handle;
 
 /* Validates shapes, allocates the device weights and a workspace for max_tokens, copies and
- * repacks the weights. Synchronous. On failure *out is set to NULL and nothing leaks. */
+ * repacks the weights. Synchronous. On failure *out is set to NULL and nothing leaks.
+ * Forwards take one of two paths (same results up to fp32 rounding; both deterministic): the
+ * decode path (three kernels, each touched expert read once per token; up to 16 tokens and
+ * 128 slots) and the batched path (tensor-core expert GEMMs, each touched expert read once for
+ * all its tokens). Forwards of fewer than 8 tokens take the decode path, larger ones the batched
+ * path when the handle has it (max_tokens >= 8 and weights within the batched path's Q2_K scale
+ * range, see DS4MOE_ERR_UNSUPPORTED_FORMAT). The environment variable DS4MOE_BATCHED_FROM, read
+ * here, replaces the 8 (17 keeps every forward the decode kernels can take on the decode path). */
 int ds4moe_create(const ds4moe_weights* w, const ds4moe_shapes* s, ds4moe_handle** out);
 
 /* Expert-parallel partial on one GPU (arc PR #89 "expert parallelism stage 0 + stage 1 (EP=2)",
@@ -164,8 +173,9 @@ int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n_tokens, const i
 
 /* As ds4moe_forward_ex with host buffers: copies x (and token_ids) to the device, runs the
  * forward and copies out back, then synchronises the stream before returning. With page-locked
- * host buffers and a decode-sized batch, the copies and the kernels replay as one cached CUDA
- * graph (keyed by the buffer addresses); pageable buffers take separate copies. */
+ * host buffers the copies and the kernels replay as one cached CUDA graph (keyed by the token
+ * counts and buffer addresses; device forwards cache their kernels' graph the same way);
+ * pageable buffers take separate copies. */
 int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t n_tokens,
                         const int32_t* token_ids_host, int32_t n_hash, float* out_host, void* stream);
 

@@ -137,6 +137,11 @@ struct ds4moe_handle {
   int n_phases = 0;
   // test of the GEMM timeout path (ds4moe_set_test_stall): stage + 1 for the next batched forward
   int test_stall = 0;
+  // Forwards of up to decode_upto tokens (and top_k slots within the decode kernels' limit) take the
+  // decode path, larger ones the batched path. The batched path reads each touched expert once for
+  // all its tokens; the decode kernels re-read it per token but launch three kernels instead of
+  // twelve. A handle without the batched path's buffers decodes up to the decode kernels' limit.
+  int decode_upto = 16;
 
   // Decode forwards replay a captured CUDA graph of their three launches (launching each kernel
   // from the host costs far more than a graph node). Graphs are keyed by the call's token
@@ -144,6 +149,7 @@ struct ds4moe_handle {
   bool use_graphs = true;
   cudaStream_t cap_stream = nullptr;
   struct GraphEntry {
+    int kind = 0;  // 0: decode path, 1: batched path
     int n = -1, n_hash = 0;
     const void* x = nullptr;
     const int* tid = nullptr;
@@ -164,8 +170,11 @@ struct ds4moe_handle {
   GraphEntry graphs[kGraphs];
   uint64_t tick = 0;
 
-  int decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int n_hash, float* out,
-                   cudaGraphExec_t* exec_out, const HostIo* io = nullptr);
+  // The graph of one forward's launches (launch(stream) returns a DS4MOE status), captured on first
+  // use for this (path, token counts, buffers) and replayed afterwards.
+  template <typename Launch>
+  int cached_graph(int kind, int n, int n_hash, const void* x, const int* tid, float* out, const HostIo* io,
+                   Launch&& launch, cudaGraphExec_t* exec_out);
   void release_graphs() {
     for (GraphEntry& g : graphs)
       if (g.exec) {
@@ -210,14 +219,15 @@ struct ds4moe_handle {
   }
 };
 
-int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const int* tid, int nh, float* o,
-                                cudaGraphExec_t* exec_out, const HostIo* io) {
+template <typename Launch>
+int ds4moe_handle::cached_graph(int kind, int n, int nh, const void* x, const int* tid, float* o, const HostIo* io,
+                                Launch&& launch, cudaGraphExec_t* exec_out) {
   const HostIo hio = io ? *io : HostIo();
   GraphEntry* hit = nullptr;
   GraphEntry* victim = &graphs[0];
   for (GraphEntry& g : graphs) {
-    if (g.exec && g.n == da.n_tok && g.n_hash == nh && g.x == x && g.tid == tid && g.out == o && g.hx == hio.x &&
-        g.htid == hio.tid && g.hout == hio.out)
+    if (g.exec && g.kind == kind && g.n == n && g.n_hash == nh && g.x == x && g.tid == tid && g.out == o &&
+        g.hx == hio.x && g.htid == hio.tid && g.hout == hio.out)
       hit = &g;
     if (!g.exec || g.used < victim->used) victim = &g;
   }
@@ -231,24 +241,26 @@ int ds4moe_handle::decode_graph(const ds4::DecodeArgs& da, const void* x, const 
     DS4_CUDA(cudaStreamBeginCapture(cap_stream, cudaStreamCaptureModeThreadLocal));
     const size_t d = (size_t)s.d;
     cudaError_t e = cudaSuccess;
-    if (hio.x) e = cudaMemcpyAsync(const_cast<void*>(x), hio.x, (size_t)da.n_tok * d * 2, cudaMemcpyHostToDevice, cap_stream);
+    int rc = DS4MOE_OK;
+    if (hio.x) e = cudaMemcpyAsync(const_cast<void*>(x), hio.x, (size_t)n * d * 2, cudaMemcpyHostToDevice, cap_stream);
     if (e == cudaSuccess && hio.tid && nh > 0)
       e = cudaMemcpyAsync(const_cast<int*>(tid), hio.tid, (size_t)nh * 4, cudaMemcpyHostToDevice, cap_stream);
-    if (e == cudaSuccess)
-      e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, true, cap_stream, nullptr, nullptr);
-    if (e == cudaSuccess && hio.out)
-      e = cudaMemcpyAsync(hio.out, o, (size_t)da.n_tok * d * 4, cudaMemcpyDeviceToHost, cap_stream);
+    if (e == cudaSuccess) rc = launch(cap_stream);
+    if (e == cudaSuccess && rc == DS4MOE_OK && hio.out)
+      e = cudaMemcpyAsync(hio.out, o, (size_t)n * d * 4, cudaMemcpyDeviceToHost, cap_stream);
     cudaError_t e2 = cudaStreamEndCapture(cap_stream, &graph);
-    if (e != cudaSuccess || e2 != cudaSuccess) {
+    if (e != cudaSuccess || e2 != cudaSuccess || rc != DS4MOE_OK) {
       if (graph) cudaGraphDestroy(graph);
       cudaGetLastError();
-      return fail(DS4MOE_ERR_CUDA, "decode graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
+      if (rc != DS4MOE_OK) return rc;
+      return fail(DS4MOE_ERR_CUDA, "forward graph capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
     }
     cudaGraphExec_t exec = nullptr;
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
-    if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode graph instantiate: %s", cudaGetErrorString(e));
-    victim->n = da.n_tok;
+    if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "forward graph instantiate: %s", cudaGetErrorString(e));
+    victim->kind = kind;
+    victim->n = n;
     victim->n_hash = nh;
     victim->x = x;
     victim->tid = tid;
@@ -471,6 +483,12 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
   ds4moe_handle* h = new ds4moe_handle();
   h->s = *s;
   if (const char* ev = getenv("DS4MOE_NO_GRAPHS")) h->use_graphs = ev[0] == '0';
+  // fewest tokens that take the batched path (measured on GB300 at d = 4096, 256 experts top-8,
+  // f = 2048: the decode path is faster up to 6 tokens, the batched path from 8: 298 vs 319 us at
+  // 8 tokens, 392 vs 599 us at 16); DS4MOE_BATCHED_FROM overrides it (17: decode path up to the
+  // decode kernels' limit of 16 tokens)
+  int small_batch_from = 8;
+  if (const char* ev = getenv("DS4MOE_BATCHED_FROM")) small_batch_from = std::max(1, atoi(ev));
   const int E = s->n_experts, d = s->d, f = s->f_routed, fs = s->f_shared, K = s->top_k;
   h->mb_gu = ds4::matrix_bytes(s->fmt_gate_up, f, d);
   h->mb_d = ds4::matrix_bytes(s->fmt_down, d, f);
@@ -527,7 +545,20 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
     DS4_TRY(h->alloc_t(&h->Hs, Md * fs * 4));
     DS4_TRY(h->alloc_t(&h->hsg, Md * (size_t)(fs / 16) * 4));
   }
-  h->has_prefill = M > (size_t)ds4::decode_max_tokens() || slots > (size_t)ds4::decode_max_slots();
+  // The batched path is needed beyond the decode kernels' limits, and serves smaller forwards from
+  // small_batch_from tokens on when the weights allow its fp16 dequantization (a handle that only
+  // needs it for small forwards falls back to the decode path rather than refusing the weights).
+  const bool need_batched = M > (size_t)ds4::decode_max_tokens() || slots > (size_t)ds4::decode_max_slots();
+  h->has_prefill = need_batched;
+  bool scales_checked = false;
+  if (!need_batched && M >= (size_t)small_batch_from) {
+    const int sc = check_q2k_scales(h);
+    if (sc == DS4MOE_OK)
+      h->has_prefill = scales_checked = true;
+    else if (sc != DS4MOE_ERR_UNSUPPORTED_FORMAT)
+      DS4_TRY(sc);
+  }
+  if (h->has_prefill) h->decode_upto = small_batch_from - 1;
   if (h->has_prefill) {
     DS4_TRY(h->alloc_t(&h->Y, slots * d * 4));
     DS4_TRY(h->alloc_t(&h->Xs16, M * d * 2));
@@ -548,7 +579,7 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
     if (!tr) tr = ds4::make_act_maps(&h->tm_h, h->H16, slots, f);
     if (!tr && s->n_shared) tr = ds4::make_act_maps(&h->tm_hs, h->Hs16, M, fs);
     if (tr) DS4_TRY(fail(DS4MOE_ERR_CUDA, "tensor map encoding failed (%d)", tr));
-    DS4_TRY(check_q2k_scales(h));
+    if (!scales_checked) DS4_TRY(check_q2k_scales(h));
     DS4_TRY(h->alloc_t(&h->router_w3, (size_t)3 * E * d * 2));
     ds4::launch_router_split(h->router_w, (size_t)E * d, h->router_w3, 0);
   }
@@ -565,6 +596,7 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
   cudaError_t e = ds4::decode_prepare();
   if (e == cudaSuccess) e = ds4::gemm_prepare();
   if (e == cudaSuccess) e = ds4::router_tc_prepare();
+  if (e == cudaSuccess) e = ds4::router_logits_prepare();
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->counts, 0, (size_t)E * 4);
   if (e == cudaSuccess) e = cudaMemset(h->n_active, 0, 4);
@@ -613,7 +645,7 @@ static ds4::DecodeArgs decode_args(ds4moe_handle* h, const __nv_bfloat16* xb, in
 }
 
 static bool is_decode(const ds4moe_handle* h, int n) {
-  return n <= ds4::decode_max_tokens() && n * h->s.top_k <= ds4::decode_max_slots();
+  return n <= h->decode_upto && n <= ds4::decode_max_tokens() && n * h->s.top_k <= ds4::decode_max_slots();
 }
 
 // Host memory that is page-locked (a graph may copy from and to it). Asked of the driver on every
@@ -627,72 +659,24 @@ static bool host_pinned(const void* p) {
   return at.type == cudaMemoryTypeHost;
 }
 
-extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, const int32_t* token_ids,
-                                 int32_t n_hash, float* out, void* stream) {
-  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+// Tokens up to which the batched path routes with the fp32 FMA router kernel.
+constexpr int kSmallRouterTokens = 32;
+
+// The batched path's launches on stream st (router, top-k, bucketing, activation prep and gather,
+// tile list, the expert GEMMs, combine); mark(name) follows each launch.
+template <typename Mark>
+static int batched_launches(ds4moe_handle* h, const __nv_bfloat16* xb, int n, const int32_t* token_ids, int n_hash,
+                            float* out, cudaStream_t st, Mark&& mark) {
   const ds4moe_shapes& s = h->s;
-  if (n < 0) return fail(DS4MOE_ERR_INVALID_ARG, "n_tokens=%d is negative", n);
-  if (n > s.max_tokens) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d exceeds max_tokens=%d", n, s.max_tokens);
-  if (n_hash < 0 || n_hash > n) return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d must be in 0..n_tokens", n_hash);
-  if (n_hash > 0 && (s.hash_vocab == 0 || !token_ids))
-    return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d needs a handle with a hash table and token_ids", n_hash);
-  if (n == 0) return DS4MOE_OK;
-  if (!x || !out) return fail(DS4MOE_ERR_INVALID_ARG, "x or out is NULL");
-  if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return fail(DS4MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
-  const void* ptrs[3] = {x, out, n_hash ? token_ids : nullptr};
-  const char* names[3] = {"x", "out", "token_ids"};
-  for (int i = 0; i < 3; ++i) {
-    if (!ptrs[i]) continue;
-    bool seen = false;  // pointers already verified on this handle skip the driver query
-    for (const void* p : h->checked)
-      if (p == ptrs[i]) seen = true;
-    if (seen) continue;
-    const PtrKind k = classify(ptrs[i], s.device);
-    if (k == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than the handle's (%d)", names[i], s.device);
-    if (k != PTR_DEVICE) return fail(DS4MOE_ERR_INVALID_ARG, "%s is not device memory (use ds4moe_forward_host for host buffers)", names[i]);
-    h->checked[h->checked_next++ % ds4moe_handle::kChecked] = ptrs[i];
-  }
-  DeviceGuard guard(s.device);
-  if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", s.device);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int E = s.n_experts, K = s.top_k, d = s.d, f = s.f_routed, fs = s.f_shared;
   const int n_learned = n - n_hash;
-  const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  int phase = 0;
-  if (h->profile) DS4_CUDA(cudaEventRecord(h->ev[0], st));
-  auto mark = [&](const char* name) {
-    if (h->profile && phase < ds4moe_handle::kMaxPhases) {
-      h->phase_name[phase] = name;
-      cudaEventRecord(h->ev[++phase], st);
-    }
-  };
-  if (n <= ds4::decode_max_tokens() && n * K <= ds4::decode_max_slots()) {
-    // decode path: three kernels, chained with programmatic dependent launch unless profiling
-    const ds4::DecodeArgs da = decode_args(h, xb, n, token_ids, n_hash, out);
-    struct Ctx {
-      decltype(mark)* m;
-    } ctx{&mark};
-    ds4::DecodeHooks hooks{[](void* c, const char* name) { (*static_cast<Ctx*>(c)->m)(name); }, &ctx};
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    DS4_CUDA(cudaStreamIsCapturing(st, &cap));
-    if (h->profile || cap != cudaStreamCaptureStatusNone || !h->use_graphs) {
-      // direct launches (also when the caller is capturing its own graph)
-      cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, !h->profile, st, nullptr,
-                                         h->profile ? &hooks : nullptr);
-      if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    } else {
-      cudaGraphExec_t exec = nullptr;
-      int rc = h->decode_graph(da, x, token_ids, n_hash, out, &exec);
-      if (rc != DS4MOE_OK) return rc;
-      DS4_CUDA(cudaGraphLaunch(exec, st));
-    }
-    h->n_phases = phase;
-    h->last_stream = st;
-    h->last_n = n;
-    return DS4MOE_OK;
-  }
   if (n_learned > 0) {
-    ds4::launch_router_tc(xb + (size_t)n_hash * d, n_learned, d, h->router_w3, h->router_b, E, h->logits, st);
+    // a few tokens: the fp32 FMA router (one warp per expert); more: the tensor-core router, whose
+    // tiles cover 64 experts each and would leave most SMs idle
+    if (n_learned <= kSmallRouterTokens)
+      ds4::launch_router_logits(xb + (size_t)n_hash * d, n_learned, d, h->router_w, h->router_b, E, h->logits, st);
+    else
+      ds4::launch_router_tc(xb + (size_t)n_hash * d, n_learned, d, h->router_w3, h->router_b, E, h->logits, st);
     mark("router_logits");
   }
   DS4_CUDA(cudaMemsetAsync(h->err, 0, 4, st));
@@ -703,7 +687,6 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   ds4::launch_bucket_scatter(h->idx, n * K, E, h->ghist, h->local_of, h->counts, h->offsets, h->active, h->n_active,
                              h->perm, h->rowof, st);
   mark("bucket_scatter");
-  if (!h->has_prefill) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d needs the batched path, not sized at create", n);
   ds4::launch_xprep(xb, n, d, h->Xs16, h->inv_s, st);
   mark("xprep");
   ds4::launch_gather(h->Xs16, h->inv_s, h->perm, h->offsets + E, n * K, K, d, h->Xp16, h->inv_p, st);
@@ -746,8 +729,85 @@ extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, con
   }
   ds4::launch_combine(h->idx, h->wts, h->rowof, h->Y, s.n_shared ? h->Ys : nullptr, n, K, d, out, st);
   mark("combine");
-  h->n_phases = phase;
   DS4_CUDA(cudaGetLastError());
+  return DS4MOE_OK;
+}
+
+extern "C" int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n, const int32_t* token_ids,
+                                 int32_t n_hash, float* out, void* stream) {
+  if (!h) return fail(DS4MOE_ERR_INVALID_ARG, "handle is NULL");
+  const ds4moe_shapes& s = h->s;
+  if (n < 0) return fail(DS4MOE_ERR_INVALID_ARG, "n_tokens=%d is negative", n);
+  if (n > s.max_tokens) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d exceeds max_tokens=%d", n, s.max_tokens);
+  if (n_hash < 0 || n_hash > n) return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d must be in 0..n_tokens", n_hash);
+  if (n_hash > 0 && (s.hash_vocab == 0 || !token_ids))
+    return fail(DS4MOE_ERR_INVALID_ARG, "n_hash=%d needs a handle with a hash table and token_ids", n_hash);
+  if (n == 0) return DS4MOE_OK;
+  if (!x || !out) return fail(DS4MOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return fail(DS4MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  const void* ptrs[3] = {x, out, n_hash ? token_ids : nullptr};
+  const char* names[3] = {"x", "out", "token_ids"};
+  for (int i = 0; i < 3; ++i) {
+    if (!ptrs[i]) continue;
+    bool seen = false;  // pointers already verified on this handle skip the driver query
+    for (const void* p : h->checked)
+      if (p == ptrs[i]) seen = true;
+    if (seen) continue;
+    const PtrKind k = classify(ptrs[i], s.device);
+    if (k == PTR_OTHER_DEVICE) return fail(DS4MOE_ERR_DEVICE_MISMATCH, "%s lives on another device than the handle's (%d)", names[i], s.device);
+    if (k != PTR_DEVICE) return fail(DS4MOE_ERR_INVALID_ARG, "%s is not device memory (use ds4moe_forward_host for host buffers)", names[i]);
+    h->checked[h->checked_next++ % ds4moe_handle::kChecked] = ptrs[i];
+  }
+  DeviceGuard guard(s.device);
+  if (!guard.ok) return fail(DS4MOE_ERR_CUDA, "cannot select device %d", s.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  int phase = 0;
+  if (h->profile) DS4_CUDA(cudaEventRecord(h->ev[0], st));
+  auto mark = [&](const char* name) {
+    if (h->profile && phase < ds4moe_handle::kMaxPhases) {
+      h->phase_name[phase] = name;
+      cudaEventRecord(h->ev[++phase], st);
+    }
+  };
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DS4_CUDA(cudaStreamIsCapturing(st, &cap));
+  // direct launches when profiling, when graphs are off, and when the caller is capturing its own graph
+  const bool direct = h->profile || cap != cudaStreamCaptureStatusNone || !h->use_graphs;
+  cudaGraphExec_t exec = nullptr;
+  if (is_decode(h, n)) {
+    // decode path: three kernels, chained with programmatic dependent launch unless profiling
+    const ds4::DecodeArgs da = decode_args(h, xb, n, token_ids, n_hash, out);
+    if (direct) {
+      struct Ctx {
+        decltype(mark)* m;
+      } ctx{&mark};
+      ds4::DecodeHooks hooks{[](void* c, const char* name) { (*static_cast<Ctx*>(c)->m)(name); }, &ctx};
+      cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, !h->profile, st, nullptr,
+                                         h->profile ? &hooks : nullptr);
+      if (e != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    } else {
+      int rc = h->cached_graph(0, n, n_hash, x, token_ids, out, nullptr, [&](cudaStream_t cs) {
+        const cudaError_t e = ds4::launch_decode(da, s.fmt_gate_up, s.fmt_down, s.fmt_shared, true, cs, nullptr, nullptr);
+        return e == cudaSuccess ? (int)DS4MOE_OK : fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+      }, &exec);
+      if (rc != DS4MOE_OK) return rc;
+      DS4_CUDA(cudaGraphLaunch(exec, st));
+    }
+  } else {
+    if (!h->has_prefill) return fail(DS4MOE_ERR_CAPACITY, "n_tokens=%d needs the batched path, not sized at create", n);
+    if (direct || h->test_stall) {  // (the timeout test's one-shot setting is not captured)
+      int rc = batched_launches(h, xb, n, token_ids, n_hash, out, st, mark);
+      if (rc != DS4MOE_OK) return rc;
+    } else {
+      int rc = h->cached_graph(1, n, n_hash, x, token_ids, out, nullptr, [&](cudaStream_t cs) {
+        return batched_launches(h, xb, n, token_ids, n_hash, out, cs, [](const char*) {});
+      }, &exec);
+      if (rc != DS4MOE_OK) return rc;
+      DS4_CUDA(cudaGraphLaunch(exec, st));
+    }
+  }
+  h->n_phases = phase;
   h->last_stream = st;
   h->last_n = n;
   return DS4MOE_OK;
@@ -773,17 +833,30 @@ extern "C" int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t
   const size_t d = (size_t)h->s.d;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   DS4_CUDA(cudaStreamIsCapturing(st, &cap));
-  if (is_decode(h, n) && h->use_graphs && !h->profile && cap == cudaStreamCaptureStatusNone &&
-      host_pinned(x_host) && host_pinned(out_host) && (n_hash == 0 || host_pinned(tid_host))) {
-    // one graph: host -> device copies, the decode kernels, device -> host copy
-    const ds4::DecodeArgs da = decode_args(h, reinterpret_cast<const __nv_bfloat16*>(h->x_stage), n,
-                                           n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage);
+  if (h->use_graphs && !h->profile && !h->test_stall && cap == cudaStreamCaptureStatusNone &&
+      (is_decode(h, n) || h->has_prefill) && host_pinned(x_host) && host_pinned(out_host) &&
+      (n_hash == 0 || host_pinned(tid_host))) {
+    // one graph: host -> device copies, the forward's kernels, device -> host copy
+    const auto* xs = reinterpret_cast<const __nv_bfloat16*>(h->x_stage);
+    const int* ts = n_hash > 0 ? h->tid_stage : nullptr;
     ds4moe_handle::HostIo io;
     io.x = x_host;
     io.tid = n_hash > 0 ? tid_host : nullptr;
     io.out = out_host;
     cudaGraphExec_t exec = nullptr;
-    int rc = h->decode_graph(da, h->x_stage, n_hash > 0 ? h->tid_stage : nullptr, n_hash, h->out_stage, &exec, &io);
+    int rc;
+    if (is_decode(h, n)) {
+      const ds4::DecodeArgs da = decode_args(h, xs, n, ts, n_hash, h->out_stage);
+      rc = h->cached_graph(0, n, n_hash, h->x_stage, ts, h->out_stage, &io, [&](cudaStream_t cs) {
+        const cudaError_t e = ds4::launch_decode(da, h->s.fmt_gate_up, h->s.fmt_down, h->s.fmt_shared, true, cs, nullptr,
+                                                 nullptr);
+        return e == cudaSuccess ? (int)DS4MOE_OK : fail(DS4MOE_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+      }, &exec);
+    } else {
+      rc = h->cached_graph(1, n, n_hash, h->x_stage, ts, h->out_stage, &io, [&](cudaStream_t cs) {
+        return batched_launches(h, xs, n, ts, n_hash, h->out_stage, cs, [](const char*) {});
+      }, &exec);
+    }
     if (rc != DS4MOE_OK) return rc;
     DS4_CUDA(cudaGraphLaunch(exec, st));
     DS4_CUDA(cudaStreamSynchronize(st));
@@ -830,8 +903,7 @@ extern "C" int64_t ds4moe_device_bytes(const ds4moe_handle* h) { return h ? h->b
 
 extern "C" int32_t ds4moe_launches_per_forward(const ds4moe_handle* h, int32_t n_tokens) {
   if (!h || n_tokens <= 0) return 0;
-  if (n_tokens <= ds4::decode_max_tokens() && n_tokens * h->s.top_k <= ds4::decode_max_slots())
-    return 3;  // route, gate/up, down + combine
+  if (is_decode(h, n_tokens)) return 3;  // route, gate/up, down + combine
   // router, top-k, 2 bucketing, activation prep + gather, tile list, routed gate/up and down GEMMs,
   // the same for the shared expert, combine
   return 1 + 1 + 2 + 2 + 1 + 2 + (h->s.n_shared ? 2 : 0) + 1;

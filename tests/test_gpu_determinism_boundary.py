@@ -88,7 +88,7 @@ def test_token_count_edges():
         assert all(sorted(r) == sorted(want.tolist()) for r in idx.tolist())
         assert np.all(got == 0.0)  # zero input -> zero expert outputs
         # a single token and a token count that is not a multiple of the pass size
-        for n in (1, 6, 16, 17, 63):  # decode path up to 16 tokens, the batched path above
+        for n in (1, 6, 8, 16, 17, 63):  # decode path below 8 tokens, the batched path from 8
             xb = synthetic.activations(SMALL_MIX, n)
             got, idx, _ = moe_gpu.forward(h, p, x_bits=xb, n_hash=min(n, 5))
             ref = moe.forward(p, x_bits=xb, n_hash=min(n, 5))
@@ -205,6 +205,35 @@ def test_q2k_scale_beyond_fp16_dequant_range_is_refused():
     assert ei.value.code == api.DS4MOE_ERR_UNSUPPORTED_FORMAT
     h = moe_gpu.create(q, max_tokens=4)  # decode path only: no fp16 dequant, accepted
     api.ds4moe_destroy(h)
+    # up to 16 tokens the decode kernels can serve every forward: such a handle accepts the
+    # weights too and keeps its 16-token forwards on the decode path
+    h = moe_gpu.create(q, max_tokens=16)
+    try:
+        assert api.ds4moe_launches_per_forward(h, 16) == 3
+    finally:
+        api.ds4moe_destroy(h)
+
+
+@pytest.mark.parametrize("batched_from", [None, "17"], ids=["default", "decode-up-to-16"])
+def test_path_selection_and_the_decode_kernels_up_to_16_tokens(monkeypatch, batched_from):
+    """Below 8 tokens a forward takes the decode path (3 launches), from 8 tokens the batched
+    path (12); with DS4MOE_BATCHED_FROM=17 at create the decode kernels serve up to 16 tokens.
+    Every token count matches the oracle either way."""
+    if batched_from:
+        monkeypatch.setenv("DS4MOE_BATCHED_FROM", batched_from)
+    spec = synthetic.CONFIGS[2]  # decode-16: d=4096, 256 experts top-8
+    p = synthetic.make_problem(spec)
+    h = moe_gpu.create(p, max_tokens=16)
+    ref = moe.forward(p)["out"]  # tokens are independent: a forward of the first n rows gives ref[:n]
+    try:
+        for n in (1, 7, 8, 16):
+            want = 3 if (batched_from or n < 8) else 12
+            assert api.ds4moe_launches_per_forward(h, n) == want, n
+            xb = np.ascontiguousarray(p.x_bits[:n])
+            got, _, _ = moe_gpu.forward(h, p, x_bits=xb, n_hash=min(n, spec.n_hash))
+            assert np.max(np.abs(got - ref[:n])) <= moe_gpu.tolerance(ref[:n]), n
+    finally:
+        api.ds4moe_destroy(h)
 
 
 def test_batched_forward_with_every_token_table_routed():

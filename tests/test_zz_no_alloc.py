@@ -21,7 +21,8 @@ SPECS = [
     synthetic.Spec("noalloc-route", d=1024, n_experts=64, top_k=6, f=256, f_shared=256, n_shared=1,
                    fmt_gate_up="q2_k", fmt_down="q2_k", fmt_shared="q8_0", n_tokens=48, seed=31, bias="normal"),
     # the full router shape (d=4096, 256 experts, top-8; 64 KB of staged activations per CTA, above
-    # the default shared-memory limit) with 16 tokens: the handle routes them on its decode path
+    # the default shared-memory limit) with 16 tokens: the handle routes them on its batched path
+    # (fp32 FMA router below 33 tokens)
     synthetic.Spec("noalloc-ds-shape", d=4096, n_experts=256, top_k=8, f=256, f_shared=256, n_shared=1,
                    fmt_gate_up="q2_k", fmt_down="q2_k", fmt_shared="q8_0", n_tokens=16, seed=32, bias="normal"),
 ]
