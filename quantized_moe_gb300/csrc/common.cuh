@@ -208,16 +208,20 @@ struct GemmArgs {
                            // of the timeout path: the MMA's wait for that stage runs out)
 };
 
-// Largest token tile the expert GEMM takes for a weight format (FMT_*).
-int gemm_tile_n(int fmt);
+// Tile geometry of the expert GEMMs for a forward (0: 192-token tiles; 1: 128-token tiles with
+// 256-k pipeline stages, for batches whose experts average fewer than 64 tokens when every GEMM's
+// K, whose greatest common divisor is k_gcd, is a multiple of 256), and its token tile (the routed
+// tiling of a forward must use the same geometry as its GEMM launches).
+int gemm_geometry(int n_tokens, int top_k, int n_experts, int k_gcd);
+int gemm_tile_n(int geom);
 cudaError_t gemm_prepare();
-// TMA maps of one row-major fp16 activation buffer: 64 columns x 64 rows and x 128 rows per box
-// (a tile's rows are fetched with as few boxes as the two sizes allow).
+// TMA maps of one row-major fp16 activation buffer: boxes of 64 columns x 16, 32, 64 and 128 rows
+// (a tile's rows are fetched exactly, with as few boxes as these sizes allow).
 struct ActMaps {
   CUtensorMap r16, r32, r64, r128;  // boxes of 64 columns x 16 / 32 / 64 / 128 rows
 };
 cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int m_tiles, int n_tiles,
-                        cudaStream_t s);
+                        int geom, cudaStream_t s);
 int make_act_maps(ActMaps* tm, const void* base, uint64_t rows, uint64_t cols);
 
 // Prefill preparation (see prefill_prep.cu).

@@ -1,6 +1,7 @@
 // C-ABI shim of the ds4moe library: argument validation, device memory, create-time repack
 // and the launch sequence of one forward. Host code only; kernels live in the other units.
 #include <algorithm>
+#include <numeric>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -280,11 +281,10 @@ namespace {
 
 bool fmt_ok(int f) { return f == DS4MOE_FMT_Q8_0 || f == DS4MOE_FMT_Q2_K; }
 
-// Token tile of the routed expert GEMMs: the gate/up and the down GEMM share one tiling, so it is
-// the smaller of the two formats' tiles.
-int routed_tile_n(const ds4moe_shapes& s) {
-  return std::min(ds4::gemm_tile_n(s.fmt_gate_up), ds4::gemm_tile_n(s.fmt_down));
-}
+// Token tile of the routed expert GEMMs of a forward (the gate/up and the down GEMM share one
+// tiling), and the largest number of routed tiles a forward of n tokens can have with it.
+int routed_tile_n(int geom) { return ds4::gemm_tile_n(geom); }
+size_t max_routed_tiles(size_t slots, int n_experts, int tn) { return (slots + tn - 1) / tn + std::min<size_t>(n_experts, slots); }
 
 int check_shapes(const ds4moe_shapes* s) {
   // the router stages 8 token rows of d bf16 values in shared memory: d <= 12288 keeps that under 200 KB
@@ -566,8 +566,7 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
     DS4_TRY(h->alloc_t(&h->H16, slots * f * 2));
     DS4_TRY(h->alloc_t(&h->inv_s, M * 4));
     DS4_TRY(h->alloc_t(&h->inv_p, slots * 4));
-    const int tn = routed_tile_n(*s);
-    const size_t max_tiles = (slots + tn - 1) / tn + E;
+    const size_t max_tiles = std::max(max_routed_tiles(slots, E, routed_tile_n(0)), max_routed_tiles(slots, E, routed_tile_n(1)));
     DS4_TRY(h->alloc_t(&h->tiles, max_tiles * sizeof(int4)));
     DS4_TRY(h->alloc_t(&h->n_tiles, 4));
     if (s->n_shared) {
@@ -691,10 +690,12 @@ static int batched_launches(ds4moe_handle* h, const __nv_bfloat16* xb, int n, co
   mark("xprep");
   ds4::launch_gather(h->Xs16, h->inv_s, h->perm, h->offsets + E, n * K, K, d, h->Xp16, h->inv_p, st);
   mark("gather");
-  const int TN = routed_tile_n(s);  // one tiling serves the gate/up and the down GEMM
+  const int k_gcd = std::gcd(std::gcd(d, f), s.n_shared ? fs : d);  // the K of every GEMM of the forward
+  const int geom = ds4::gemm_geometry(n, K, E, k_gcd);
+  const int TN = routed_tile_n(geom);  // one tiling serves the gate/up and the down GEMM
   ds4::launch_tiles(h->counts, h->offsets, E, h->local_of, TN, h->tiles, h->n_tiles, st);
   mark("tiles");
-  const int routed_tiles = (n * K + TN - 1) / TN + std::min(E, n * K), dense_tiles = (n + TN - 1) / TN;
+  const int routed_tiles = (int)max_routed_tiles((size_t)n * K, E, TN), dense_tiles = (n + TN - 1) / TN;
   ds4::GemmArgs g{};
   g.w0 = h->gate; g.w1 = h->up; g.mat_bytes = h->mb_gu; g.k = d; g.tiles = h->tiles; g.n_tiles = h->n_tiles;
   g.inv_scale = h->inv_p; g.h_out = h->H16; g.ld_out = f; g.err = h->err;
@@ -703,27 +704,27 @@ static int batched_launches(ds4moe_handle* h, const __nv_bfloat16* xb, int n, co
     g.timeout_cycles = 2000000;
     h->test_stall = 0;
   }
-  cudaError_t ge = ds4::launch_gemm(s.fmt_gate_up, true, h->tm_xp, g, f / 64, routed_tiles, st);
+  cudaError_t ge = ds4::launch_gemm(s.fmt_gate_up, true, h->tm_xp, g, f / 64, routed_tiles, geom, st);
   if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(ge));
   mark("routed_gateup");
   if (s.n_shared) {
     ds4::GemmArgs gs{};
     gs.w0 = h->sgate; gs.w1 = h->sup; gs.k = d; gs.n_rows = n; gs.inv_scale = h->inv_s; gs.h_out = h->Hs16;
     gs.ld_out = fs; gs.err = h->err;
-    ge = ds4::launch_gemm(s.fmt_shared, true, h->tm_xs, gs, fs / 64, dense_tiles, st);
+    ge = ds4::launch_gemm(s.fmt_shared, true, h->tm_xs, gs, fs / 64, dense_tiles, geom, st);
     if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "shared gate/up GEMM launch: %s", cudaGetErrorString(ge));
     mark("shared_gateup");
   }
   ds4::GemmArgs gd{};
   gd.w0 = h->down; gd.mat_bytes = h->mb_d; gd.k = f; gd.tiles = h->tiles; gd.n_tiles = h->n_tiles;
   gd.y_out = h->Y; gd.ld_out = d; gd.err = h->err;
-  ge = ds4::launch_gemm(s.fmt_down, false, h->tm_h, gd, d / 128, routed_tiles, st);
+  ge = ds4::launch_gemm(s.fmt_down, false, h->tm_h, gd, d / 128, routed_tiles, geom, st);
   if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "down GEMM launch: %s", cudaGetErrorString(ge));
   mark("routed_down");
   if (s.n_shared) {
     ds4::GemmArgs gsd{};
     gsd.w0 = h->sdown; gsd.k = fs; gsd.n_rows = n; gsd.y_out = h->Ys; gsd.ld_out = d; gsd.err = h->err;
-    ge = ds4::launch_gemm(s.fmt_shared, false, h->tm_hs, gsd, d / 128, dense_tiles, st);
+    ge = ds4::launch_gemm(s.fmt_shared, false, h->tm_hs, gsd, d / 128, dense_tiles, geom, st);
     if (ge != cudaSuccess) return fail(DS4MOE_ERR_CUDA, "shared down GEMM launch: %s", cudaGetErrorString(ge));
     mark("shared_down");
   }

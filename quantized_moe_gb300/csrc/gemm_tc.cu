@@ -47,50 +47,51 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BK = 64;  // BK: K of one 128-byte swizzled sub-tile (64 fp16)
-#ifndef GEMM_SUB
-#define GEMM_SUB 2
-#endif
-constexpr int SUB = GEMM_SUB;  // sub-tiles per pipeline stage: 8 MMAs between a wait and a commit
-constexpr int SK = SUB * BK;   // K of one pipeline stage
 constexpr int kDeqWarps = 16;
 constexpr int kDeqGroups = 4;  // groups of four warps (one per TMEM lane quadrant)
 constexpr int kFirstDeq = 3;   // warps 0-2: weight producer, MMA, activation producer
 constexpr int kEpiWarps = 4;   // warps 19-22: epilogue, one per TMEM lane quadrant
 constexpr int kThreads = (kFirstDeq + kDeqWarps + kEpiWarps) * 32;  // 736
-
-#ifndef GEMM_BN
-#define GEMM_BN 192
-#endif
-// Tensor memory: two accumulators of BN fp32 columns, then the A stages (SK of fp16 = SK / 2
-// columns) in the columns left over.
-constexpr int ACC_COLS = GEMM_BN;
-constexpr int A_COLS = SK / 2;
-constexpr int A_COL0 = 2 * ACC_COLS;
 constexpr int TMEM_COLS = 512;
-#ifndef GEMM_ASTAGES
-#define GEMM_ASTAGES ((TMEM_COLS - 2 * GEMM_BN) / A_COLS < 8 ? (TMEM_COLS - 2 * GEMM_BN) / A_COLS : 8)
-#endif
-constexpr int A_STAGES = GEMM_ASTAGES;
-static_assert(A_COL0 + A_STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
 
-template <int FMT>
+// Two tile geometries, chosen per forward (gemm_geometry): token tile BN (the MMA's N at most),
+// sub-tiles per pipeline stage SUB, activation stages and raw weight units in flight.
+//   0 (wide):  BN = 192, SUB = 2: for batches whose experts average 64 tokens or more;
+//   1 (small): BN = 128, SUB = 4: 16 MMAs per barrier wait and commit. With few tokens per expert
+//              the MMA warp's per-stage loop, not the tensor pipe or HBM, bounds a stage, and a
+//              256-k stage halves the number of stages (measured: decode-16 gate/up 0.197 ->
+//              0.172 ms, prefill-512 0.452 -> 0.427 ms; prefill-4096 would lose 28 %: experts
+//              above 128 tokens would be dequantized twice).
+template <int GEOM>
+struct Geo;
+template <>
+struct Geo<0> {
+  static constexpr int BN = 192, SUB = 2, BS_Q2K = 3, BS_Q80 = 3;
+};
+template <>
+struct Geo<1> {
+  static constexpr int BN = 128, SUB = 4, BS_Q2K = 2, BS_Q80 = 2;
+};
+
+template <int FMT, int GEOM>
 struct Cfg {
+  static constexpr int BN = Geo<GEOM>::BN;      // token tile
+  static constexpr int SUB = Geo<GEOM>::SUB;    // 64-k sub-tiles per pipeline stage
+  static constexpr int SK = SUB * BK;           // K of one pipeline stage
+  // Tensor memory: two accumulators of BN fp32 columns, then the A stages (SK of fp16 = SK / 2
+  // columns) in the columns left over.
+  static constexpr int ACC_COLS = BN;
+  static constexpr int A_COLS = SK / 2;
+  static constexpr int A_COL0 = 2 * ACC_COLS;
+  static constexpr int A_STAGES = (TMEM_COLS - A_COL0) / A_COLS < 8 ? (TMEM_COLS - A_COL0) / A_COLS : 8;
+  static_assert(A_STAGES >= 2 && A_COL0 + A_STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
   static constexpr int RAW_BYTES = 8 * unit_bytes(FMT);  // one K unit of the 128-row tile
-#ifndef GEMM_RAWS_Q2K
-#define GEMM_RAWS_Q2K 4
-#endif
-  static constexpr int RAWS = FMT == FMT_Q2_K ? GEMM_RAWS_Q2K : 4;  // K units in flight
-  // Token tile (MMA N at most): 192 tokens.
-  static constexpr int BN = GEMM_BN;
-  static constexpr int SUB_BYTES = BN * BK * 2;  // one 64-k sub-tile
+  static constexpr int RAWS = 4;                         // K units in flight
+  static constexpr int SUB_BYTES = BN * BK * 2;          // one 64-k activation sub-tile
   static constexpr int B_BYTES = SUB * SUB_BYTES;
-  // activation stages in shared memory, one per A stage in tensor memory
-#ifndef GEMM_BSTAGES_Q2K
-#define GEMM_BSTAGES_Q2K 3
-#endif
-  // activation stages: more than the A stages, so that the TMA of a stage is issued well before
-  // the MMA needs it (an L2 read under load takes around a thousand cycles)
-  static constexpr int B_STAGES = FMT == FMT_Q2_K ? GEMM_BSTAGES_Q2K : 3;
+  // activation stages: more than the A stages where shared memory allows, so that the TMA of a
+  // stage is issued well before the MMA needs it (an L2 read under load takes ~a thousand cycles)
+  static constexpr int B_STAGES = FMT == FMT_Q2_K ? Geo<GEOM>::BS_Q2K : Geo<GEOM>::BS_Q80;
   static constexpr int OFF_B = 0;
   static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
   static_assert(BN <= 256 && BN % 16 == 0, "token tile");
@@ -250,13 +251,15 @@ __device__ __forceinline__ int item_count(const GemmArgs& p) {
 // of CS): each loads its share of the rows of every activation stage and multicasts it to all,
 // and each MMA commit releases the stage in all of them, so the activation tile crosses L2 once
 // per cluster.
-template <int FMT, bool GATEUP, int CS>
+template <int FMT, bool GATEUP, int CS, int GEOM>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap16,
                                                                       const __grid_constant__ CUtensorMap tmap32,
                                                                       const __grid_constant__ CUtensorMap tmap64,
                                                                       const __grid_constant__ CUtensorMap tmap128,
                                                                       GemmArgs p) {
-  using C = Cfg<FMT>;
+  using C = Cfg<FMT, GEOM>;
+  constexpr int SUB = C::SUB, SK = C::SK, A_STAGES = C::A_STAGES, A_COLS = C::A_COLS, A_COL0 = C::A_COL0;
+  constexpr int ACC_COLS = C::ACC_COLS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -414,9 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
         tc_fence_after();
         const uint32_t ta = tmem + (uint32_t)(A_COL0 + st * A_COLS);
         const uint32_t bsm = su32(smem + C::OFF_B + sb * C::B_BYTES);
-        // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of a B sub-tile
-        static_assert(SUB == 2, "the stage's MMAs are issued as one block of eight");
-        tc_mma8_ts_elect(acc, ta, sw128_desc(bsm), sw128_desc(bsm + C::SUB_BYTES), idesc, s != 0);
+        // 16 fp16 of K per MMA: 8 TMEM columns of A, 32 bytes of a B sub-tile; blocks of eight
+        static_assert(SUB % 2 == 0, "the stage's MMAs are issued in blocks of eight (two sub-tiles)");
+#pragma unroll
+        for (int h = 0; h < SUB / 2; ++h)
+          tc_mma8_ts_elect(acc, ta + 64 * h, sw128_desc(bsm + 2 * h * C::SUB_BYTES),
+                           sw128_desc(bsm + (2 * h + 1) * C::SUB_BYTES), idesc, (s | h) != 0);
         tc_commit2_elect(&b.b_empty[sb], CS > 1 ? kMask : 0, &b.a_empty[st]);
       }
       if (!ok) break;
@@ -550,12 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_tc_kernel(const __gri
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int FMT, bool GATEUP, int CS>
+template <int FMT, bool GATEUP, int CS, int GEOM>
 cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<FMT>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<FMT, GEOM>::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -564,16 +570,16 @@ cudaError_t launch_one(const ActMaps& tm, const GemmArgs& p, int grid, cudaStrea
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CS > 1 ? 1 : 0;  // a plain launch without clusters
-  return cudaLaunchKernelEx(&cfg, expert_gemm_tc_kernel<FMT, GATEUP, CS>, tm.r16, tm.r32, tm.r64, tm.r128, p);
+  return cudaLaunchKernelEx(&cfg, expert_gemm_tc_kernel<FMT, GATEUP, CS, GEOM>, tm.r16, tm.r32, tm.r64, tm.r128, p);
 }
 
 // Clusters of CS CTAs that can be resident at once (0 if none).
-template <int FMT, bool GATEUP, int CS>
+template <int FMT, bool GATEUP, int CS, int GEOM>
 int max_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * CS);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<FMT>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<FMT, GEOM>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CS;
@@ -582,54 +588,79 @@ int max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_tc_kernel<FMT, GATEUP, CS>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_tc_kernel<FMT, GATEUP, CS, GEOM>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <int FMT, bool GATEUP, int CS>
+template <int FMT, bool GATEUP, int CS, int GEOM>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<FMT>::SMEM_BYTES);
+  return cudaFuncSetAttribute(expert_gemm_tc_kernel<FMT, GATEUP, CS, GEOM>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FMT, GEOM>::SMEM_BYTES);
 }
 
-template <int FMT, bool GATEUP>
-cudaError_t prepare_fmt(int* pairs, int* quads) {
-  cudaError_t e = prepare_one<FMT, GATEUP, 1>();
-  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 2>();
-  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 4>();
-  *pairs = e == cudaSuccess ? max_clusters<FMT, GATEUP, 2>() : 0;
-  *quads = e == cudaSuccess ? max_clusters<FMT, GATEUP, 4>() : 0;
+// Per device, geometry and (format, gate/up or down) kernel: resident clusters of two and four.
+int g_pairs[64][2][4], g_quads[64][2][4];
+
+template <int FMT, bool GATEUP, int GEOM>
+cudaError_t prepare_fmt(int dev, int k) {
+  cudaError_t e = prepare_one<FMT, GATEUP, 1, GEOM>();
+  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 2, GEOM>();
+  if (e == cudaSuccess) e = prepare_one<FMT, GATEUP, 4, GEOM>();
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    g_pairs[dev][GEOM][k] = max_clusters<FMT, GATEUP, 2, GEOM>();
+    g_quads[dev][GEOM][k] = max_clusters<FMT, GATEUP, 4, GEOM>();
+  }
   return e;
 }
 
-// Per device: resident clusters of two and of four for each (format, gate/up or down) kernel.
-int g_pairs[64][4], g_quads[64][4];
+template <int GEOM>
+cudaError_t prepare_geom(int dev) {
+  cudaError_t e = prepare_fmt<FMT_Q2_K, true, GEOM>(dev, 0);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q2_K, false, GEOM>(dev, 1);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, true, GEOM>(dev, 2);
+  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, false, GEOM>(dev, 3);
+  return e;
+}
+
+template <int CS, int GEOM>
+cudaError_t launch_cs(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int grid, cudaStream_t s) {
+  if (fmt == FMT_Q2_K)
+    return gateup ? launch_one<FMT_Q2_K, true, CS, GEOM>(tm, p, grid, s)
+                  : launch_one<FMT_Q2_K, false, CS, GEOM>(tm, p, grid, s);
+  return gateup ? launch_one<FMT_Q8_0, true, CS, GEOM>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, CS, GEOM>(tm, p, grid, s);
+}
+
+template <int GEOM>
+cudaError_t launch_geom(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int items, int m_tiles, int sms,
+                        int dev, cudaStream_t s) {
+  const bool known = dev >= 0 && dev < 64;
+  const int k = (fmt == FMT_Q2_K ? 0 : 2) + (gateup ? 0 : 1);
+  const int quads = known ? g_quads[dev][GEOM][k] : 0, pairs = known ? g_pairs[dev][GEOM][k] : 0;
+  if (!p.tiles && m_tiles % 4 == 0 && quads > 0)
+    return launch_cs<4, GEOM>(fmt, gateup, tm, p, 4 * std::max(1, std::min(quads, items / 4)), s);
+  if (m_tiles % 2 == 0 && pairs > 0)
+    return launch_cs<2, GEOM>(fmt, gateup, tm, p, 2 * std::max(1, std::min(pairs, items / 2)), s);
+  return launch_cs<1, GEOM>(fmt, gateup, tm, p, std::max(1, std::min(sms, items)), s);
+}
 
 }  // namespace
 
-int gemm_tile_n(int fmt) { return fmt == FMT_Q2_K ? Cfg<FMT_Q2_K>::BN : Cfg<FMT_Q8_0>::BN; }
+int gemm_tile_n(int geom) { return geom ? Geo<1>::BN : Geo<0>::BN; }
+
+int gemm_geometry(int n_tokens, int top_k, int n_experts, int k_gcd) {
+  // fewer than 64 tokens per expert on average, and every K a multiple of the 256-k stage
+  return (int64_t)n_tokens * top_k < 64ll * n_experts && k_gcd % (Geo<1>::SUB * BK) == 0 ? 1 : 0;
+}
 
 cudaError_t gemm_prepare() {
   int dev = 0;
   cudaGetDevice(&dev);
-  int scratch[8];
-  int* pairs = (dev >= 0 && dev < 64) ? g_pairs[dev] : scratch;
-  int* quads = (dev >= 0 && dev < 64) ? g_quads[dev] : scratch + 4;
-  cudaError_t e = prepare_fmt<FMT_Q2_K, true>(&pairs[0], &quads[0]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q2_K, false>(&pairs[1], &quads[1]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, true>(&pairs[2], &quads[2]);
-  if (e == cudaSuccess) e = prepare_fmt<FMT_Q8_0, false>(&pairs[3], &quads[3]);
+  cudaError_t e = prepare_geom<0>(dev);
+  if (e == cudaSuccess) e = prepare_geom<1>(dev);
   return e;
-}
-
-template <int CS>
-cudaError_t launch_cs(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p, int grid, cudaStream_t s) {
-  if (fmt == FMT_Q2_K)
-    return gateup ? launch_one<FMT_Q2_K, true, CS>(tm, p, grid, s) : launch_one<FMT_Q2_K, false, CS>(tm, p, grid, s);
-  return gateup ? launch_one<FMT_Q8_0, true, CS>(tm, p, grid, s) : launch_one<FMT_Q8_0, false, CS>(tm, p, grid, s);
 }
 
 // Persistent launch: one CTA per SM (at most), each looping over the (token tile, weight slice)
@@ -638,7 +669,7 @@ cudaError_t launch_cs(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& p
 // for the dense (shared expert) GEMMs, of two for the routed ones (measured: clusters of four leave
 // more SMs idle than the routed GEMMs gain from the smaller activation traffic).
 cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs& args, int m_tiles, int n_tiles,
-                        cudaStream_t s) {
+                        int geom, cudaStream_t s) {
   static int n_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -648,13 +679,8 @@ cudaError_t launch_gemm(int fmt, bool gateup, const ActMaps& tm, const GemmArgs&
   GemmArgs p = args;
   p.m_tiles = m_tiles;
   const int items = m_tiles * n_tiles;
-  const int k = (fmt == FMT_Q2_K ? 0 : 2) + (gateup ? 0 : 1);
-  const int quads = known ? g_quads[dev][k] : 0, pairs = known ? g_pairs[dev][k] : 0;
-  if (!args.tiles && m_tiles % 4 == 0 && quads > 0)
-    return launch_cs<4>(fmt, gateup, tm, p, 4 * std::max(1, std::min(quads, items / 4)), s);
-  if (m_tiles % 2 == 0 && pairs > 0)
-    return launch_cs<2>(fmt, gateup, tm, p, 2 * std::max(1, std::min(pairs, items / 2)), s);
-  return launch_cs<1>(fmt, gateup, tm, p, std::max(1, std::min(sms, items)), s);
+  return geom ? launch_geom<1>(fmt, gateup, tm, p, items, m_tiles, sms, dev, s)
+              : launch_geom<0>(fmt, gateup, tm, p, items, m_tiles, sms, dev, s);
 }
 
 // fp16 2D tensor map over a row-major [rows x cols] buffer, boxes of 64 columns x box_rows rows
