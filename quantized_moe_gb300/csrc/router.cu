@@ -6,7 +6,7 @@ namespace ds4 {
 namespace {
 
 constexpr int kRouterTok = 8;    // tokens per CTA
-constexpr int kRouterWarps = 8;  // one expert per warp
+constexpr int kRouterWarps = 8;  // one expert per warp (measured: four per CTA was slower)
 
 // logits[t][e] = sum_k x[t][k] * W_r[e][k] + b[e], fp32 products and sums.
 __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x, int n_tok, int d,
@@ -30,17 +30,26 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 #pragma unroll
   for (int tt = 0; tt < kRouterTok; ++tt) acc[tt] = 0.f;
   const float* wr = w + (size_t)e * d;
-  for (int k0 = lane * 4; k0 < d; k0 += 128) {
-    const float4 wv = *reinterpret_cast<const float4*>(wr + k0);
+  // four weight loads in flight per lane before their FMAs (d is a multiple of 128); the products
+  // are summed in the same order as one k step after another
+  for (int k0 = lane * 4; k0 < d; k0 += 512) {
+    float4 wv[4];
 #pragma unroll
-    for (int tt = 0; tt < kRouterTok; ++tt) {
-      const uint2 xv = *reinterpret_cast<const uint2*>(xs + tt * d + k0);
-      const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
-      const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
-      acc[tt] = fmaf(wv.x, x01.x, acc[tt]);
-      acc[tt] = fmaf(wv.y, x01.y, acc[tt]);
-      acc[tt] = fmaf(wv.z, x23.x, acc[tt]);
-      acc[tt] = fmaf(wv.w, x23.y, acc[tt]);
+    for (int u = 0; u < 4; ++u)
+      wv[u] = k0 + 128 * u < d ? *reinterpret_cast<const float4*>(wr + k0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (k0 + 128 * u >= d) break;
+#pragma unroll
+      for (int tt = 0; tt < kRouterTok; ++tt) {
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + tt * d + k0 + 128 * u);
+        const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
+        const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
+        acc[tt] = fmaf(wv[u].x, x01.x, acc[tt]);
+        acc[tt] = fmaf(wv[u].y, x01.y, acc[tt]);
+        acc[tt] = fmaf(wv[u].z, x23.x, acc[tt]);
+        acc[tt] = fmaf(wv[u].w, x23.y, acc[tt]);
+      }
     }
   }
   const float bias = b ? b[e] : 0.f;
@@ -211,7 +220,7 @@ void launch_router_logits(const __nv_bfloat16* x, int n_tok, int d, const float*
                           float* logits, cudaStream_t s) {
   const size_t smem = (size_t)kRouterTok * d * sizeof(__nv_bfloat16);
   dim3 grid((n_tok + kRouterTok - 1) / kRouterTok, (n_exp + kRouterWarps - 1) / kRouterWarps);
-  router_logits_kernel<<<grid, 256, smem, s>>>(x, n_tok, d, w, b, n_exp, logits);
+  router_logits_kernel<<<grid, 32 * kRouterWarps, smem, s>>>(x, n_tok, d, w, b, n_exp, logits);
 }
 
 // The kernel stages up to 8 x 12288 bf16 activations (192 KB) in shared memory. Function
