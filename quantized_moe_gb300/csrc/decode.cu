@@ -27,6 +27,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 256;
+// the one-token top-k of the route kernel ranks one expert per thread (n_experts <= 256)
+static_assert(kThreads >= 256, "route kernel: one thread per expert");
 constexpr int kMaxTok = 16;
 constexpr int kMaxSlots = 128;
 constexpr int kMaxJ = 12;  // d <= 12288: float4 loads per lane of one router row slice
