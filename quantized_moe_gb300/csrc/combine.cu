@@ -36,35 +36,38 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ id
     s_n = n;
   }
   __syncthreads();
-  // 1024 columns per CTA (one float4 per thread); the slot loop is unrolled with predicated loads
-  // so that all of a column's loads are in flight together (the fixed order of the sum is kept)
-  const int i4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i4 >= d) return;
+  // the slot loop is unrolled with predicated loads so that all of a column's loads are in flight
+  // together (the fixed order of the sum is kept); small batches spread a row over several CTAs
   const int n = s_n;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4; i4 < d; i4 += gridDim.x * blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < n) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4));  // read once
-      const float w = s_w[j];
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < n) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s_pos[j] * d + i4));  // read once
+        const float w = s_w[j];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
     }
+    if (ys) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(ys + (size_t)t * d + i4));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    __stcs(reinterpret_cast<float4*>(out + (size_t)t * d + i4), acc);
   }
-  if (ys) {
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(ys + (size_t)t * d + i4));
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-  }
-  __stcs(reinterpret_cast<float4*>(out + (size_t)t * d + i4), acc);
 }
 
 }  // namespace
 
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s) {
-  combine_kernel<<<dim3((d + 1023) / 1024, n_tok), 256, 0, s>>>(idx, wts, rowof, y, ys, top_k, d, out);
+  // up to 256 tokens a row is split over CTAs of 1024 columns (more CTAs than tokens); beyond, one CTA
+  // per token row (measured at 4096 tokens: 123 us vs 128 us with the split)
+  const int split = n_tok <= 256 ? (d + 1023) / 1024 : 1;
+  combine_kernel<<<dim3(split, n_tok), 256, 0, s>>>(idx, wts, rowof, y, ys, top_k, d, out);
 }
 
 }  // namespace ds4
