@@ -14,8 +14,9 @@ for phase k that lands while an earlier phase is still open is counted in that e
 `simulate` replays the committed protocol under random interleavings and random completion delays
 and asserts, for every wait, that its barrier had reached the phase it waits for (no parity
 aliasing) and, for every arrival and copy, that it lands in the phase it belongs to. The constants
-are the kernel's: two A stages, three B stages, two sub-tiles per stage, raw rings of four units
-(Q2_K units hold four sub-tiles, Q8_0 units two), clusters of one, two and four CTAs.
+are the kernel's two geometries (two A stages with three B stages and two sub-tiles per stage, or
+two A and two B stages with four sub-tiles per stage), raw rings of four units (Q2_K units hold
+four sub-tiles, Q8_0 units two), clusters of one, two and four CTAs.
 `simulate_single_ring` replays the earlier one-ring protocol; with it the last tests show that the
 model does catch a dequant group that skips its release wait, and the split-ring variant that
 faulted on the GPU (six A stages over three B stages, dequant groups waiting for the B tile).
@@ -329,12 +330,16 @@ def simulate(kpu, raws, n_items, stages_per_item, seed, cs=1, a_stages=2, b_stag
     return ctas
 
 
+@pytest.mark.parametrize("geom,sub,a_stages,b_stages", [("wide", 2, 2, 3), ("small", 4, 2, 2)])
 @pytest.mark.parametrize("cs", [1, 2, 4])
 @pytest.mark.parametrize("fmt,kpu", [("q2_k", 4), ("q8_0", 2)])
-def test_committed_protocol_has_no_parity_alias(fmt, kpu, cs):
-    for seed in range(60):
-        # K = 512: four pipeline stages (eight sub-tiles) per item, three items
-        simulate(kpu, raws=4, n_items=3, stages_per_item=4, seed=seed, cs=cs)
+def test_committed_protocol_has_no_parity_alias(fmt, kpu, cs, geom, sub, a_stages, b_stages):
+    # the kernel's two tile geometries: 192-token tiles with two sub-tiles per stage, three
+    # activation stages; 128-token tiles with four sub-tiles per stage, two activation stages
+    for seed in range(40):
+        # four pipeline stages per item, three items
+        simulate(kpu, raws=4, n_items=3, stages_per_item=4, seed=seed, cs=cs, a_stages=a_stages,
+                 b_stages=b_stages, sub=sub)
 
 
 def test_committed_protocol_with_short_items():
