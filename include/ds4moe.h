@@ -174,8 +174,10 @@ int ds4moe_forward_ex(ds4moe_handle* h, const void* x, int32_t n_tokens, const i
 /* As ds4moe_forward_ex with host buffers: copies x (and token_ids) to the device, runs the
  * forward and copies out back, then synchronises the stream before returning. With page-locked
  * host buffers the copies and the kernels replay as one cached CUDA graph (keyed by the token
- * counts and buffer addresses; device forwards cache their kernels' graph the same way);
- * pageable buffers take separate copies. */
+ * counts and buffer addresses; device forwards cache their kernels' graph the same way), and x and
+ * out (when 16-byte aligned) are copied by a kernel that addresses them directly rather than by
+ * the copy engines (DS4MOE_SM_COPIES=0 at create turns that off); pageable buffers take separate
+ * copies. */
 int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t n_tokens,
                         const int32_t* token_ids_host, int32_t n_hash, float* out_host, void* stream);
 

@@ -1,6 +1,8 @@
 // Deterministic combine: out[t] = sum over the token's routed slots, in ascending expert id,
 // of w_j * Y[position of slot j], then + the shared expert's row, all fp32, no atomics. Slots
 // without a bucketed position (experts the handle does not hold) contribute nothing.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace ds4 {
@@ -60,7 +62,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ id
   }
 }
 
+// dst[i] = src[i] for `bytes` bytes (16-byte aligned), with 16-byte loads and stores: a copy run by
+// the SMs, for buffers in page-locked host memory that kernels address directly.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                     size_t n16) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __ldcs(src + i);
+}
+
 }  // namespace
+
+void launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  const int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
+  copy16_kernel<<<std::max(blocks, 1), 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+}
 
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s) {

@@ -166,7 +166,12 @@ struct ds4moe_handle {
     const void* x = nullptr;
     const int* tid = nullptr;
     float* out = nullptr;
+    // the same x and out as kernels address them (page-locked memory under unified addressing),
+    // or null: copied by the SMs instead of the copy engines when present
+    const void* x_k = nullptr;
+    float* out_k = nullptr;
   };
+  bool sm_copies = true;
   static constexpr int kGraphs = 16;
   GraphEntry graphs[kGraphs];
   uint64_t tick = 0;
@@ -243,12 +248,21 @@ int ds4moe_handle::cached_graph(int kind, int n, int nh, const void* x, const in
     const size_t d = (size_t)s.d;
     cudaError_t e = cudaSuccess;
     int rc = DS4MOE_OK;
-    if (hio.x) e = cudaMemcpyAsync(const_cast<void*>(x), hio.x, (size_t)n * d * 2, cudaMemcpyHostToDevice, cap_stream);
+    if (hio.x && hio.x_k) {
+      ds4::launch_copy16(hio.x_k, const_cast<void*>(x), (size_t)n * d * 2, cap_stream);
+      e = cudaGetLastError();
+    } else if (hio.x) {
+      e = cudaMemcpyAsync(const_cast<void*>(x), hio.x, (size_t)n * d * 2, cudaMemcpyHostToDevice, cap_stream);
+    }
     if (e == cudaSuccess && hio.tid && nh > 0)
       e = cudaMemcpyAsync(const_cast<int*>(tid), hio.tid, (size_t)nh * 4, cudaMemcpyHostToDevice, cap_stream);
     if (e == cudaSuccess) rc = launch(cap_stream);
-    if (e == cudaSuccess && rc == DS4MOE_OK && hio.out)
+    if (e == cudaSuccess && rc == DS4MOE_OK && hio.out && hio.out_k) {
+      ds4::launch_copy16(o, hio.out_k, (size_t)n * d * 4, cap_stream);
+      e = cudaGetLastError();
+    } else if (e == cudaSuccess && rc == DS4MOE_OK && hio.out) {
       e = cudaMemcpyAsync(hio.out, o, (size_t)n * d * 4, cudaMemcpyDeviceToHost, cap_stream);
+    }
     cudaError_t e2 = cudaStreamEndCapture(cap_stream, &graph);
     if (e != cudaSuccess || e2 != cudaSuccess || rc != DS4MOE_OK) {
       if (graph) cudaGraphDestroy(graph);
@@ -483,6 +497,7 @@ static int create_impl(const ds4moe_weights* w, const ds4moe_shapes* s_in, const
   ds4moe_handle* h = new ds4moe_handle();
   h->s = *s;
   if (const char* ev = getenv("DS4MOE_NO_GRAPHS")) h->use_graphs = ev[0] == '0';
+  if (const char* ev = getenv("DS4MOE_SM_COPIES")) h->sm_copies = ev[0] != '0';
   // fewest tokens that take the batched path (measured on GB300 at d = 4096, 256 experts top-8,
   // f = 2048: the decode path is faster up to 6 tokens, the batched path from 8: 298 vs 319 us at
   // 8 tokens, 392 vs 599 us at 16); DS4MOE_BATCHED_FROM overrides it (17: decode path up to the
@@ -656,6 +671,18 @@ static bool host_pinned(const void* p) {
     return false;
   }
   return at.type == cudaMemoryTypeHost;
+}
+
+// The address by which kernels reach page-locked host memory (null if they cannot, or if it is not
+// 16-byte aligned).
+static void* kernel_view(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer || ((uintptr_t)at.devicePointer & 15)) return nullptr;
+  return at.devicePointer;
 }
 
 // Tokens up to which the batched path routes with the fp32 FMA router kernel.
@@ -844,6 +871,10 @@ extern "C" int ds4moe_forward_host(ds4moe_handle* h, const void* x_host, int32_t
     io.x = x_host;
     io.tid = n_hash > 0 ? tid_host : nullptr;
     io.out = out_host;
+    if (h->sm_copies) {
+      io.x_k = kernel_view(x_host);
+      io.out_k = static_cast<float*>(kernel_view(out_host));
+    }
     cudaGraphExec_t exec = nullptr;
     int rc;
     if (is_decode(h, n)) {
