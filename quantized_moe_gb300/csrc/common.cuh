@@ -248,9 +248,6 @@ int bucket_chunks(int n_slots);  // ints of the bucketing scratch: bucket_chunks
 void launch_bucket_count(const int* idx, int n_slots, int n_exp, const int* local_of, int* ghist, cudaStream_t s);
 void launch_bucket_scatter(const int* idx, int n_slots, int n_exp, const int* ghist, const int* local_of, int* counts,
                            int* offsets, int* active, int* n_active, int* perm, int* rowof, cudaStream_t s);
-// A 16-byte-vector copy run by the SMs (bytes a multiple of 16, both pointers 16-byte aligned and
-// addressable by kernels: device memory or page-locked host memory under unified addressing).
-void launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 void launch_combine(const int* idx, const float* wts, const int* rowof, const float* y, const float* ys, int n_tok,
                     int top_k, int d, float* out, cudaStream_t s);
 

@@ -63,6 +63,10 @@ PtrKind classify(const void* p, int device) {
 namespace ds4 {
 // Lets the other translation units report errors through ds4moe_last_error.
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+// A 16-byte-vector copy run by the SMs (combine.cu; bytes a multiple of 16, both pointers 16-byte
+// aligned and addressable by kernels: device memory or page-locked host memory under unified
+// addressing).
+void launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 }  // namespace ds4
 
 struct ds4moe_handle {
