@@ -5,12 +5,14 @@
 //                         the last CTA to finish (atomic arrival counter, no waiting) runs the
 //                         sigmoid top-k (or table routing), the bucketing, and publishes a work
 //                         list (expert, first position, count) per active expert, the token of
-//                         every bucketed position and the fp16 scale of every token. Further CTAs
-//                         (one per 16 rows of f_shared) compute the shared expert's gate/up, which
-//                         needs no routing, alongside the router.
+//                         every bucketed position and the fp16 scale of every token. It lets the
+//                         gate/up kernel launch at once.
 //  gateup_decode_kernel   CTA = 16 rows of f of one active expert, K split over 8 warps, each warp
 //                         streaming its units through a two-deep register pipeline; h = silu(g) * u
-//                         in fp32 plus max|h| per row of H (integer atomicMax: order-free).
+//                         in fp32 plus max|h| per row of H (integer atomicMax: order-free). Its first
+//                         grid row computes the shared expert's gate/up (one CTA per 16 rows of
+//                         f_shared): it needs no routing, so those CTAs do not wait for the route
+//                         kernel and overlap it; the routed CTAs wait for it.
 //  down_decode_kernel     CTA = 16 rows of d for every touched expert and the shared expert;
 //                         (expert, K unit) items are dealt round-robin to the warps, each warp
 //                         accumulates its partials in shared memory in a fixed order, and the
@@ -43,14 +45,10 @@ constexpr int kPass = 1;
 template <int FMT_S>
 __device__ void shared_gateup_cta(const DecodeArgs& a, int rg);
 
-template <int FMT_S>
 __global__ void __launch_bounds__(kThreads, 2) route_decode_kernel(DecodeArgs a) {
-  // CTAs past the routed experts compute the shared expert's gate/up, which needs no routing: it
-  // overlaps the router and its serial top-k tail instead of following them.
-  if ((int)blockIdx.x >= a.n_exp) {
-    shared_gateup_cta<FMT_S>(a, blockIdx.x - a.n_exp);
-    return;
-  }
+  // The gate/up kernel may launch now: its shared-expert CTAs need no routing and overlap this
+  // kernel (its routed CTAs wait for this grid to complete).
+  pdl_trigger();
   __shared__ float part[kWarps][kMaxTok];
   __shared__ float xmx[kWarps][kMaxTok];
   __shared__ int s_last;
@@ -470,16 +468,21 @@ __device__ __forceinline__ void gu_epilogue(float (&red)[kWarps][2][P][16], cons
   __syncthreads();
 }
 
-template <int FMT_R, int P>
+template <int FMT_R, int FMT_S, int P>
 __global__ void __launch_bounds__(kThreads, 2) gateup_decode_kernel(DecodeArgs a, int max_active) {
   __shared__ float red[kWarps][2][P][16];
   const int rg = blockIdx.x, warp = threadIdx.x >> 5;
+  if (a.n_shared && blockIdx.y == 0) {  // the shared expert (row group rg): no routing, no wait
+    pdl_trigger();
+    shared_gateup_cta<FMT_S>(a, rg);
+    return;
+  }
   const BMask bm;
   const Q2kLaneConst qc;
   if (rg * 16 >= a.f) return;
   pdl_wait();
   pdl_trigger();
-  const int4 wk = a.work[blockIdx.y];  // expert, first position, count (0 past the active ones)
+  const int4 wk = a.work[blockIdx.y - (a.n_shared ? 1 : 0)];  // expert, first position, count (0 past the active ones)
   const int e = wk.x, pos0 = wk.y, cnt = wk.z;
   if (cnt == 0) return;
   const uint8_t* w0 = a.gate + (size_t)e * a.mb_gu;
@@ -505,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_decode_kernel(DecodeArgs a
 }
 
 // The shared expert's gate/up for 16 rows (row group rg of f_shared) and every token, run by the
-// route kernel's extra CTAs. The token scales are computed here (the router's CTA 0 publishes
-// them only for the routed kernels); max|h| of the 16 rows goes to hsg[token][rg] (the down
-// kernel reduces over the row groups).
+// gate/up kernel's first grid row without waiting for the route kernel. The token scales are
+// computed here (the router's CTA 0 publishes them only after the routing); max|h| of the 16 rows
+// goes to hsg[token][rg] (the down kernel reduces over the row groups).
 template <int FMT_S>
 __device__ void shared_gateup_cta(const DecodeArgs& a, int rg) {
   constexpr int P = kPass;
@@ -863,9 +866,9 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, size_t smem, cudaStream_t s, bool 
   return cudaLaunchKernelEx(&cfg, kernel, a, max_active);
 }
 
-template <int R>
+template <int R, int S>
 cudaError_t launch_gu(dim3 grid, cudaStream_t s, bool pdl, const DecodeArgs& a, int max_active) {
-  return launch_ex(gateup_decode_kernel<R, kPass>, grid, 0, s, pdl, a, max_active);
+  return launch_ex(gateup_decode_kernel<R, S, kPass>, grid, 0, s, pdl, a, max_active);
 }
 
 template <int R, int S, int P>
@@ -899,18 +902,19 @@ int decode_max_slots() { return kMaxSlots; }
 cudaError_t launch_decode(const DecodeArgs& a, int fmt_r_gu, int fmt_r_d, int fmt_s, bool pdl, cudaStream_t s,
                           int* launches, const DecodeHooks* hooks) {
   const int max_active = min(a.n_exp, a.n_tok * a.top_k);
-  // the routed experts' router CTAs, then the shared expert's gate/up CTAs (one per 16 rows)
-  const int route_grid = a.n_exp + (a.n_shared ? a.fs / 16 : 0);
-  if (a.n_shared && fmt_s == FMT_Q2_K)
-    route_decode_kernel<FMT_Q2_K><<<route_grid, kThreads, 0, s>>>(a);
-  else
-    route_decode_kernel<FMT_Q8_0><<<route_grid, kThreads, 0, s>>>(a);
+  route_decode_kernel<<<a.n_exp, kThreads, 0, s>>>(a);  // one CTA per routed expert
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "route");
-  const dim3 g_gu(a.f / 16, max_active);
-  e = fmt_r_gu == FMT_Q2_K ? launch_gu<FMT_Q2_K>(g_gu, s, pdl, a, max_active)
-                           : launch_gu<FMT_Q8_0>(g_gu, s, pdl, a, max_active);
+  // row y = 0: the shared expert's row groups (when it exists); rows 1..: the active experts
+  const int fsg = a.n_shared ? fmt_s : fmt_r_gu;
+  const dim3 g_gu(max(a.f, a.n_shared ? a.fs : 0) / 16, max_active + (a.n_shared ? 1 : 0));
+  if (fmt_r_gu == FMT_Q2_K)
+    e = fsg == FMT_Q2_K ? launch_gu<FMT_Q2_K, FMT_Q2_K>(g_gu, s, pdl, a, max_active)
+                        : launch_gu<FMT_Q2_K, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
+  else
+    e = fsg == FMT_Q2_K ? launch_gu<FMT_Q8_0, FMT_Q2_K>(g_gu, s, pdl, a, max_active)
+                        : launch_gu<FMT_Q8_0, FMT_Q8_0>(g_gu, s, pdl, a, max_active);
   if (e != cudaSuccess) return e;
   if (hooks) hooks->mark(hooks->ctx, "gateup");
   const int fsd = a.n_shared ? fmt_s : fmt_r_d;
