@@ -30,13 +30,20 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 #pragma unroll
   for (int tt = 0; tt < kRouterTok; ++tt) acc[tt] = 0.f;
   const float* wr = w + (size_t)e * d;
-  // four weight loads in flight per lane before their FMAs (d is a multiple of 128); the products
-  // are summed in the same order as one k step after another
+  // four weight loads per lane and step (d is a multiple of 128), the next step's issued before
+  // this step's FMAs; the products are summed in the same order as one k step after another
+  float4 nx[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    nx[u] = lane * 4 + 128 * u < d ? *reinterpret_cast<const float4*>(wr + lane * 4 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k0 = lane * 4; k0 < d; k0 += 512) {
     float4 wv[4];
 #pragma unroll
+    for (int u = 0; u < 4; ++u) wv[u] = nx[u];
+#pragma unroll
     for (int u = 0; u < 4; ++u)
-      wv[u] = k0 + 128 * u < d ? *reinterpret_cast<const float4*>(wr + k0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      nx[u] = k0 + 512 + 128 * u < d ? *reinterpret_cast<const float4*>(wr + k0 + 512 + 128 * u)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (k0 + 128 * u >= d) break;
