@@ -25,6 +25,14 @@ SMALL_Q8_NOSHARED = synthetic.Spec("small-q8-noshared", d=384, n_experts=12, top
                                    n_tokens=21, seed=22)
 MIXED_FMT = synthetic.Spec("mixed-fmt", d=512, n_experts=8, top_k=2, f=256, f_shared=256, n_shared=1,
                            fmt_gate_up="q8_0", fmt_down="q2_k", fmt_shared="q2_k", n_tokens=9, seed=23)
+# Decode path (fewer than 8 tokens) with the shared expert wider, then narrower, than the routed
+# experts: the gate/up launch spans the wider of the two, and the other's CTAs past its rows exit.
+DECODE_WIDE_SHARED = synthetic.Spec("decode-wide-shared", d=512, n_experts=16, top_k=4, f=256, f_shared=384,
+                                    n_shared=1, fmt_gate_up="q2_k", fmt_down="q2_k", fmt_shared="q8_0",
+                                    n_tokens=5, seed=25, bias="normal", n_hash=1, hash_vocab=50)
+DECODE_NARROW_SHARED = synthetic.Spec("decode-narrow-shared", d=512, n_experts=16, top_k=4, f=384, f_shared=128,
+                                      n_shared=1, fmt_gate_up="q2_k", fmt_down="q8_0", fmt_shared="q8_0",
+                                      n_tokens=3, seed=26)
 # Zipf-skewed routing over 16 experts: the busiest experts take 700, 673, 550, 355, 230 ... of the
 # 700 tokens, so each spans several token tiles of the expert GEMM with a ragged last tile, and
 # the shared expert's 700 tokens end in a ragged tile as well.
@@ -94,7 +102,8 @@ def _run(spec, tokens=None, pooled=False):
 
 
 @pytest.mark.parametrize("spec", [synthetic.CONFIGS[0], synthetic.CONFIGS[1], synthetic.CONFIGS[2], SMALL_MIX,
-                                  SMALL_Q8_NOSHARED, MIXED_FMT], ids=lambda s: s.name)
+                                  SMALL_Q8_NOSHARED, MIXED_FMT, DECODE_WIDE_SHARED, DECODE_NARROW_SHARED],
+                         ids=lambda s: s.name)
 def test_full_forward_matches_oracle(spec):
     p, got, idx, w, ref = _run(spec)
     exempt = check_route(ref, idx, w, spec.n_hash, spec.top_k)
